@@ -1,0 +1,217 @@
+/*
+ * libkda — Kimi Delta Attention (KDA) recurrent decode for GB300 (sm_103a).
+ *
+ * One decode step of the KDA recurrence per (row, head) "unit".  The state
+ * S of a unit is a 128 x 128 matrix stored as S[k][v]: row = key channel,
+ * column = value channel, value channel contiguous.  With q, k L2-normalised
+ * (eps 1e-6), g the per-key-channel log decay and beta the delta-rule rate:
+ *
+ *     S_d = diag(exp(g)) S
+ *     u   = beta * (v - S_d^T k)
+ *     S'  = S_d + k u^T                  (written back in place)
+ *     o   = scale * S'^T q               (scale = 1/sqrt(128) by default)
+ *
+ * Sources, cited by page title and section:
+ *   [P1] "flashinfer.kda_decode" (module overview): the Kimi-Linear T=1 gate
+ *        -exp(A_log) * softplus(g + dt_bias), beta sigmoid and QK
+ *        normalisation in-kernel; Q, K, V may be views into one padded
+ *        projection row and raw G / beta may have independent row strides;
+ *        packed cu_seqlens form with ragged lengths and null slots
+ *        ("Frozen / speculative-verify mode").
+ *   [P2] "flashinfer.kda_decode.fused_kda_decode" (Parameters): the fused
+ *        conv + KDA + gated RMSNorm contract.
+ *   [P3] "feat(cake_kda): add serving-native packed decode backend" ("Exact
+ *        contract"): the packed Kimi K3 T=1 contract.
+ *   [P4] "feat(kda): add fused speculative decode kernel - #4809" (review
+ *        of the T=1 row mapping): token rows past the last sequence are
+ *        padding that write zero and touch no slot.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - All tensor data pointers are DEVICE memory owned by the caller.  The
+ *   library allocates nothing, never synchronises the host, and never reads
+ *   device memory on the host, so every call can be captured in a CUDA graph.
+ * - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *   stream) of the calling thread's current device, which must be a
+ *   compute-capability 10.3 (GB300) device.  An unsupported device returns
+ *   KDA_ERR_UNSUPPORTED; there is no fallback path.
+ * - Every call launches exactly one kernel.  Any contract breach (dtype,
+ *   rank, shape, stride, alignment, aliasing) is detected on the host and
+ *   returned as a status WITHOUT launching anything; kda_last_error_message()
+ *   then describes it.  A launch failure returns KDA_ERR_CUDA.
+ * - state_indices: contiguous int32, one entry per decode row.  A row whose
+ *   index is <= 0 or >= num_slots is a null row: its output is zero and no
+ *   cache slot is read or written (slot 0 is the reserved null slot).  Live
+ *   indices must be unique; that is a caller contract the library does not
+ *   check (it would need a device read).
+ * - State pool [num_slots, H, 128, 128], float32 or bfloat16: each slot's
+ *   [H, 128, 128] block is contiguous, the slot stride is any value >=
+ *   H*128*128 that keeps 16-byte alignment.  The recurrence runs in float32;
+ *   a bfloat16 state is rounded once (round-to-nearest-even) on write-back.
+ * - Outputs are bfloat16 and contiguous, rounded to nearest even.
+ * - Strides are in elements.  Activation vectors need unit stride on the
+ *   channel axis and 16-byte (float32) or 8-byte (bfloat16) aligned rows.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* bad dtype / rank / shape / stride / alignment / null pointer */
+  KDA_ERR_UNSUPPORTED = 2, /* valid request this build does not serve (device, head count) */
+  KDA_ERR_ALIAS = 3,       /* a written tensor overlaps another argument */
+  KDA_ERR_CUDA = 4         /* a CUDA runtime call or the launch failed */
+} kda_status;
+
+typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1, KDA_I32 = 2 } kda_dtype;
+
+/* A strided view of device memory.  shape/stride entries past ndim are ignored. */
+typedef struct kda_tensor {
+  void* data;        /* device address of element [0, ..., 0] */
+  int32_t dtype;     /* kda_dtype */
+  int32_t ndim;      /* 1..4 */
+  int64_t shape[4];
+  int64_t stride[4]; /* in elements */
+} kda_tensor;
+
+/*
+ * kda_recurrent_decode — T=1 recurrent decode with split q, k, v.
+ * [P1] Kimi-Linear T=1 equal-head schedules; [P2] "lower_bound" for the
+ * bounded gate.
+ *
+ *   q, k, v     [B, H, 128] or [B, 1, H, 128], float32 or bfloat16 (one dtype
+ *               for all three); any positive row and head strides.
+ *   raw_gate    same shape as q, float32 or bfloat16 (pre-gate values).
+ *   raw_beta    [B, H] or [B, 1, H], float32 or bfloat16 (logits).
+ *   A_log       [H] float32, contiguous.
+ *   dt_bias     [H*128] or [H, 128] float32, contiguous.
+ *   state_indices [B] int32, contiguous.
+ *   state       [num_slots, H, 128, 128] float32 or bfloat16, updated in place.
+ *   out         [B, H, 128] or [B, 1, H, 128] bfloat16, contiguous (written).
+ *   has_lower_bound = 0: g = -exp(A_log[h]) * softplus(raw_gate + dt_bias).
+ *   has_lower_bound = 1: g = lower_bound * sigmoid(exp(A_log[h]) * (raw_gate + dt_bias)),
+ *               lower_bound < 0.
+ *   scale       output scale (> 0), normally 1/sqrt(128).
+ */
+kda_status kda_recurrent_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                const kda_tensor* raw_gate, const kda_tensor* raw_beta,
+                                const kda_tensor* A_log, const kda_tensor* dt_bias,
+                                const kda_tensor* state_indices, const kda_tensor* state,
+                                const kda_tensor* out, int32_t has_lower_bound,
+                                float lower_bound, float scale, void* stream);
+
+/*
+ * kda_packed_decode — serving-native packed Kimi K3 T=1 decode ([P3] "Exact
+ * contract"): H = 12, K = V = 128, bfloat16 data and bfloat16 state, fixed
+ * scale 1/sqrt(128), L2 eps 1e-6 and lower_bound -5.
+ *
+ *   mixed_qkv   [B, 4608] bfloat16: q | k | v, each 12 x 128 head-major;
+ *               channel stride 1, any row stride.
+ *   raw_gate    [B, 1536] bfloat16, channel stride 1, any row stride.
+ *   raw_beta    [B, 12] bfloat16.
+ *   A_log       [12] float32;  dt_bias [1536] float32.
+ *   state_indices [B] int32 (-1 = inactive graph-padding row).
+ *   state       [num_slots, 12, 128, 128] bfloat16, updated in place.
+ *   out         [B, 1, 12, 128] or [B, 12, 128] bfloat16, contiguous.
+ */
+kda_status kda_packed_decode(const kda_tensor* mixed_qkv, const kda_tensor* raw_gate,
+                             const kda_tensor* raw_beta, const kda_tensor* A_log,
+                             const kda_tensor* dt_bias, const kda_tensor* state_indices,
+                             const kda_tensor* state, const kda_tensor* out, void* stream);
+
+/*
+ * kda_fused_decode — width-4 depthwise causal conv + SiLU, one KDA step and
+ * gated RMSNorm ([P2] "fused_kda_decode", Parameters).  conv_state and state
+ * are updated in place; null rows touch neither.
+ *
+ *   x           [rows, 3*H*128] bfloat16 packed q|k|v projection, channel stride 1.
+ *   conv_weight [3, 4, H*128] float32 contiguous (section q/k/v, tap, channel).
+ *   conv_state  [num_slots, 3*H*128, 3] bfloat16 with strides
+ *               [slot_stride, 1, 3*H*128]: cached raw samples, oldest first.
+ *   raw_gate    [1, rows, H, 128] or [rows, H, 128] bfloat16.
+ *   raw_beta    [1, rows, H] or [rows, H] bfloat16.
+ *   A_log [H], dt_bias [H*128] float32;  state_indices [rows] int32.
+ *   state       [num_slots, H, 128, 128] float32 or bfloat16 (same num_slots
+ *               as conv_state).
+ *   output_gate [rows, H, 128] or [1, rows, H, 128] bfloat16 (gate logits).
+ *   norm_weight [128] float32.
+ *   has_lower_bound / lower_bound: gate form as in kda_recurrent_decode
+ *               (the pages' default is the bounded gate with -5).
+ *   norm_eps    RMSNorm epsilon (>= 0, default 1e-5).
+ *   out         [1, rows, H, 128] or [rows, H, 128] bfloat16 contiguous:
+ *               RMSNorm(o) * norm_weight * sigmoid(output_gate).
+ */
+kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight,
+                            const kda_tensor* conv_state, const kda_tensor* raw_gate,
+                            const kda_tensor* raw_beta, const kda_tensor* A_log,
+                            const kda_tensor* dt_bias, const kda_tensor* state_indices,
+                            const kda_tensor* state, const kda_tensor* output_gate,
+                            const kda_tensor* norm_weight, int32_t has_lower_bound,
+                            float lower_bound, float norm_eps, const kda_tensor* out,
+                            void* stream);
+
+/*
+ * kda_spec_decode — packed speculative decode, T >= 1 tokens per row with
+ * ragged cu_seqlens ([P1] Cake T=1..6 family with precomputed gates and
+ * "Frozen / speculative-verify mode"'s packed cu_seqlens form; [P4] padding).
+ *
+ *   q, k, v     [R, H, 128] float32 or bfloat16 token rows (one dtype).
+ *   g           [R, H, 128] float32 precomputed log decay (<= 0).
+ *   beta        [R, H] float32 or bfloat16: logits if beta_is_logit, else rates.
+ *   cu_seqlens  [N+1] int32 contiguous, read on the device: row n owns token
+ *               rows cu[n] .. cu[n+1]-1, processed in order with the state
+ *               kept in float32 on chip; its final state goes to its slot.
+ *               Token rows outside [cu[0], cu[N]) are padding: zero output.
+ *               Rows are clamped to [0, R); empty rows do nothing.
+ *   t_max       host hint: longest row expected (>= 1); used for scheduling
+ *               only, longer rows are still processed correctly.
+ *   state_indices [N] int32;  state [num_slots, H, 128, 128] float32/bfloat16.
+ *   out         [R, H, 128] bfloat16 contiguous.
+ *   scale       output scale (> 0).
+ */
+kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                           const kda_tensor* g, const kda_tensor* beta, int32_t beta_is_logit,
+                           const kda_tensor* cu_seqlens, int32_t t_max,
+                           const kda_tensor* state_indices, const kda_tensor* state,
+                           const kda_tensor* out, float scale, void* stream);
+
+/* ---- host-only queries (no CUDA calls) ---------------------------------- */
+
+/* Operation ids for kda_plan_split. */
+typedef enum kda_op { KDA_OP_RECURRENT = 0, KDA_OP_PACKED = 1, KDA_OP_FUSED = 2, KDA_OP_SPEC = 3 } kda_op;
+
+/*
+ * Value-column split the dispatcher picks for `units` = rows * heads on a
+ * device with `sm_count` SMs (state_dtype: KDA_F32 / KDA_BF16; t_max: tokens
+ * per row, 1 for T=1).  Each CTA then owns 128/split value columns of one
+ * unit.  Returns the split (1, 2, 4, 8 or 16), or 0 on invalid arguments.
+ * Honors kda_set_split_override.
+ */
+int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max,
+                       int32_t sm_count);
+
+/*
+ * Force the split of every later call in this process (0 restores the
+ * measured policy).  For sweeps and tests.  Returns KDA_ERR_INVALID_ARG for
+ * a split this build has no kernel for (the fused entry point always uses
+ * split 1 and ignores the override).
+ */
+kda_status kda_set_split_override(int32_t split);
+
+const char* kda_status_string(kda_status s);
+/* Detail of the last non-OK status returned on the calling thread. */
+const char* kda_last_error_message(void);
+/* Library version string. */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

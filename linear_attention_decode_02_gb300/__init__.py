@@ -1,1 +1,15 @@
-"""GB300-native Kimi Delta Attention (KDA) recurrent decode."""
+"""GB300-native Kimi Delta Attention (KDA) recurrent decode.
+
+The four decode entry points of libkda, with the C names:
+
+    kda_recurrent_decode   T=1, split q/k/v, softplus or bounded gate
+    kda_packed_decode      Kimi K3 packed QKV, T=1, bf16 state
+    kda_fused_decode       short conv + SiLU, KDA step, gated RMSNorm
+    kda_spec_decode        ragged speculative rows, T >= 1 tokens each
+
+Build the library with ``python -m linear_attention_decode_02_gb300.build``.
+"""
+
+from .binding import (KdaError, kda_fused_decode, kda_packed_decode, kda_plan_split,  # noqa: F401
+                      kda_recurrent_decode, kda_set_split_override, kda_spec_decode, kda_version,
+                      library)

@@ -1,0 +1,191 @@
+"""Thin Python binding of libkda (ctypes): argument marshalling only.
+
+Each function has the name of its C entry point, turns torch tensors into
+``kda_tensor`` descriptors, passes the current CUDA stream, and raises
+``KdaError`` on any non-OK status.  All arithmetic runs in the library's
+CUDA kernels; there is no fallback path: if ``libkda.so`` is missing the
+first call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
+_lock = threading.Lock()
+_lib = None
+
+KDA_OK = 0
+STATUS_NAMES = {0: "KDA_OK", 1: "KDA_ERR_INVALID_ARG", 2: "KDA_ERR_UNSUPPORTED", 3: "KDA_ERR_ALIAS",
+                4: "KDA_ERR_CUDA"}
+OP_RECURRENT, OP_PACKED, OP_FUSED, OP_SPEC = 0, 1, 2, 3
+KDA_F32, KDA_BF16, KDA_I32 = 0, 1, 2
+_DTYPES = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16, torch.int32: KDA_I32}
+DEFAULT_SCALE = 1.0 / math.sqrt(128.0)
+
+# Every symbol include/kda.h declares.
+EXPORTS = ("kda_recurrent_decode", "kda_packed_decode", "kda_fused_decode", "kda_spec_decode",
+           "kda_plan_split", "kda_set_split_override", "kda_status_string",
+           "kda_last_error_message", "kda_version")
+
+
+class KdaError(RuntimeError):
+    """A non-OK status returned by libkda."""
+
+    def __init__(self, status, message):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class KdaTensor(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
+                ("shape", ctypes.c_int64 * 4), ("stride", ctypes.c_int64 * 4)]
+
+
+def _declare(lib):
+    T = ctypes.POINTER(KdaTensor)
+    i32, f32, vp = ctypes.c_int32, ctypes.c_float, ctypes.c_void_p
+    sigs = {
+        "kda_recurrent_decode": [T, T, T, T, T, T, T, T, T, T, i32, f32, f32, vp],
+        "kda_packed_decode": [T, T, T, T, T, T, T, T, vp],
+        "kda_fused_decode": [T, T, T, T, T, T, T, T, T, T, T, i32, f32, f32, T, vp],
+        "kda_spec_decode": [T, T, T, T, T, i32, T, i32, T, T, T, f32, vp],
+    }
+    for name, args in sigs.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.kda_plan_split.argtypes = [i32, ctypes.c_int64, i32, i32, i32]
+    lib.kda_plan_split.restype = i32
+    lib.kda_set_split_override.argtypes = [i32]
+    lib.kda_set_split_override.restype = ctypes.c_int
+    lib.kda_status_string.argtypes = [ctypes.c_int]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_last_error_message.argtypes = []
+    lib.kda_last_error_message.restype = ctypes.c_char_p
+    lib.kda_version.argtypes = []
+    lib.kda_version.restype = ctypes.c_char_p
+    return lib
+
+
+def library(path=None):
+    """Load (once) and return the ctypes handle of libkda.so."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or _LIB_PATH
+            if not os.path.exists(p):
+                raise RuntimeError(f"libkda.so is not built ({p}); run "
+                                   "`python -m linear_attention_decode_02_gb300.build`")
+            _lib = _declare(ctypes.CDLL(p))
+        return _lib
+
+
+def desc(t):
+    """kda_tensor descriptor of a torch tensor (shape and strides in elements)."""
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}")
+    if t.dim() < 1 or t.dim() > 4:
+        raise ValueError(f"rank {t.dim()} not in 1..4")
+    d = KdaTensor()
+    d.data = t.data_ptr() if t.numel() > 0 else None
+    d.dtype = _DTYPES[t.dtype]
+    d.ndim = t.dim()
+    for i, (s, st) in enumerate(zip(t.shape, t.stride())):
+        d.shape[i] = s
+        d.stride[i] = st
+    return d
+
+
+def _ref(t):
+    return ctypes.byref(desc(t))
+
+
+def _stream(t):
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _check(lib, status):
+    if status != KDA_OK:
+        raise KdaError(status, lib.kda_last_error_message().decode())
+
+
+def kda_recurrent_decode(q, k, v, raw_gate, raw_beta, A_log, dt_bias, state_indices, state,
+                         out=None, lower_bound=None, scale=DEFAULT_SCALE):
+    """T=1 recurrent decode; updates `state` in place, returns bf16 out [B, H, 128]."""
+    lib = library()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.kda_recurrent_decode(_ref(q), _ref(k), _ref(v), _ref(raw_gate), _ref(raw_beta),
+                                      _ref(A_log), _ref(dt_bias), _ref(state_indices), _ref(state),
+                                      _ref(out), int(lower_bound is not None),
+                                      float(lower_bound if lower_bound is not None else 0.0),
+                                      float(scale), _stream(q))
+    _check(lib, st)
+    return out
+
+
+def kda_packed_decode(mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, state_indices, state, out=None):
+    """Packed Kimi K3 T=1 decode; updates `state` in place, returns out [B, 1, 12, 128]."""
+    lib = library()
+    if out is None:
+        out = torch.empty((mixed_qkv.shape[0], 1, 12, 128), dtype=torch.bfloat16, device=mixed_qkv.device)
+    with torch.cuda.device(mixed_qkv.device):
+        st = lib.kda_packed_decode(_ref(mixed_qkv), _ref(raw_gate), _ref(raw_beta), _ref(A_log),
+                                   _ref(dt_bias), _ref(state_indices), _ref(state), _ref(out),
+                                   _stream(mixed_qkv))
+    _check(lib, st)
+    return out
+
+
+def kda_fused_decode(x, conv_weight, conv_state, raw_gate, raw_beta, A_log, dt_bias, state_indices,
+                     state, output_gate, norm_weight, lower_bound=-5.0, norm_eps=1e-5, out=None):
+    """Fused conv + KDA + gated RMSNorm; updates both caches, returns out [1, rows, H, 128]."""
+    lib = library()
+    if out is None:
+        H = state.shape[1]
+        out = torch.empty((1, x.shape[0], H, 128), dtype=torch.bfloat16, device=x.device)
+    with torch.cuda.device(x.device):
+        st = lib.kda_fused_decode(_ref(x), _ref(conv_weight), _ref(conv_state), _ref(raw_gate),
+                                  _ref(raw_beta), _ref(A_log), _ref(dt_bias), _ref(state_indices),
+                                  _ref(state), _ref(output_gate), _ref(norm_weight),
+                                  int(lower_bound is not None),
+                                  float(lower_bound if lower_bound is not None else 0.0),
+                                  float(norm_eps), _ref(out), _stream(x))
+    _check(lib, st)
+    return out
+
+
+def kda_spec_decode(q, k, v, g, beta, cu_seqlens, state_indices, state, t_max, out=None,
+                    beta_is_logit=True, scale=DEFAULT_SCALE):
+    """Ragged speculative decode; updates `state` in place, returns out [R, H, 128]."""
+    lib = library()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    with torch.cuda.device(q.device):
+        st = lib.kda_spec_decode(_ref(q), _ref(k), _ref(v), _ref(g), _ref(beta), int(bool(beta_is_logit)),
+                                 _ref(cu_seqlens), int(t_max), _ref(state_indices), _ref(state),
+                                 _ref(out), float(scale), _stream(q))
+    _check(lib, st)
+    return out
+
+
+def kda_plan_split(op, units, state_dtype, t_max, sm_count):
+    """Split the dispatcher picks (host-only query)."""
+    return int(library().kda_plan_split(int(op), int(units), int(state_dtype), int(t_max), int(sm_count)))
+
+
+def kda_set_split_override(split):
+    """Force every later call's split (0 restores the policy)."""
+    lib = library()
+    _check(lib, lib.kda_set_split_override(int(split)))
+
+
+def kda_version():
+    return library().kda_version().decode()

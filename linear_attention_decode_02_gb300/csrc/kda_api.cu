@@ -1,0 +1,611 @@
+// libkda C ABI: host-side contract validation, split policy and launch.
+//
+// Every entry point validates its whole contract on the host before
+// launching anything (no device reads, no allocation, no synchronisation),
+// then launches exactly one kernel on the caller's stream.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/kda.h"
+#include "kda_launch.h"
+
+namespace {
+
+constexpr int64_t kD = 128;
+constexpr int64_t kUnit = kD * kD;  // elements of one (slot, head) state block
+
+thread_local std::string g_last_error;
+std::atomic<int> g_split_override{0};
+
+kda_status fail(kda_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+#define KDA_CHECK(cond, st, ...)          \
+  do {                                    \
+    if (!(cond)) return fail(st, __VA_ARGS__); \
+  } while (0)
+
+#define KDA_TRY(expr)                \
+  do {                               \
+    kda_status s__ = (expr);         \
+    if (s__ != KDA_OK) return s__;   \
+  } while (0)
+
+int64_t esize(int32_t dtype) { return dtype == KDA_BF16 ? 2 : 4; }
+
+const char* dtname(int32_t d) {
+  switch (d) {
+    case KDA_F32: return "float32";
+    case KDA_BF16: return "bfloat16";
+    case KDA_I32: return "int32";
+    default: return "unknown";
+  }
+}
+
+// A tensor viewed with a fixed rank after dropping a leading/inner unit axis.
+struct View {
+  const char* name = nullptr;
+  char* data = nullptr;
+  int32_t dtype = -1;
+  int ndim = 0;
+  int64_t shape[4] = {0, 0, 0, 0};
+  int64_t stride[4] = {0, 0, 0, 0};
+  int64_t numel() const {
+    int64_t n = 1;
+    for (int i = 0; i < ndim; ++i) n *= shape[i];
+    return n;
+  }
+  // Byte range [lo, hi) touched by the view (all strides are positive).
+  void range(uintptr_t* lo, uintptr_t* hi) const {
+    if (numel() == 0) { *lo = *hi = 0; return; }
+    int64_t ext = 1;
+    for (int i = 0; i < ndim; ++i) ext += (shape[i] - 1) * stride[i];
+    *lo = reinterpret_cast<uintptr_t>(data);
+    *hi = *lo + static_cast<uintptr_t>(ext * esize(dtype));
+  }
+};
+
+kda_status raw_view(const kda_tensor* t, const char* name, View* v) {
+  KDA_CHECK(t != nullptr, KDA_ERR_INVALID_ARG, "%s: null tensor descriptor", name);
+  KDA_CHECK(t->ndim >= 1 && t->ndim <= 4, KDA_ERR_INVALID_ARG, "%s: ndim %d not in 1..4", name, t->ndim);
+  KDA_CHECK(t->dtype == KDA_F32 || t->dtype == KDA_BF16 || t->dtype == KDA_I32, KDA_ERR_INVALID_ARG,
+            "%s: unknown dtype %d", name, t->dtype);
+  v->name = name;
+  v->data = static_cast<char*>(t->data);
+  v->dtype = t->dtype;
+  v->ndim = t->ndim;
+  for (int i = 0; i < t->ndim; ++i) {
+    KDA_CHECK(t->shape[i] >= 0, KDA_ERR_INVALID_ARG, "%s: negative extent %lld on axis %d", name,
+              (long long)t->shape[i], i);
+    KDA_CHECK(t->stride[i] > 0 || t->shape[i] <= 1, KDA_ERR_INVALID_ARG,
+              "%s: stride %lld on axis %d must be positive", name, (long long)t->stride[i], i);
+    v->shape[i] = t->shape[i];
+    v->stride[i] = t->shape[i] <= 1 && t->stride[i] <= 0 ? 1 : t->stride[i];
+  }
+  KDA_CHECK(v->data != nullptr || v->numel() == 0, KDA_ERR_INVALID_ARG, "%s: null data pointer", name);
+  return KDA_OK;
+}
+
+// Accepts rank `want`, or rank want+1 with a unit axis at `unit_axis` (dropped).
+kda_status ranked_view(const kda_tensor* t, const char* name, int want, int unit_axis, View* v) {
+  KDA_TRY(raw_view(t, name, v));
+  if (v->ndim == want + 1 && unit_axis >= 0 && v->shape[unit_axis] == 1) {
+    for (int i = unit_axis; i < v->ndim - 1; ++i) {
+      v->shape[i] = v->shape[i + 1];
+      v->stride[i] = v->stride[i + 1];
+    }
+    v->ndim = want;
+  }
+  KDA_CHECK(v->ndim == want, KDA_ERR_INVALID_ARG, "%s: expected rank %d, got %d", name, want, t->ndim);
+  return KDA_OK;
+}
+
+kda_status need_dtype(const View& v, int32_t a, int32_t b = -1) {
+  KDA_CHECK(v.dtype == a || v.dtype == b, KDA_ERR_INVALID_ARG, "%s: dtype %s not accepted", v.name,
+            dtname(v.dtype));
+  return KDA_OK;
+}
+
+kda_status need_shape(const View& v, int axis, int64_t want) {
+  KDA_CHECK(v.shape[axis] == want, KDA_ERR_INVALID_ARG, "%s: axis %d is %lld, expected %lld", v.name, axis,
+            (long long)v.shape[axis], (long long)want);
+  return KDA_OK;
+}
+
+kda_status need_contiguous(const View& v) {
+  int64_t expect = 1;
+  for (int i = v.ndim - 1; i >= 0; --i) {
+    KDA_CHECK(v.shape[i] <= 1 || v.stride[i] == expect, KDA_ERR_INVALID_ARG, "%s: must be contiguous", v.name);
+    expect *= v.shape[i];
+  }
+  return KDA_OK;
+}
+
+// Activation vectors [rows, heads, 128]: channel stride 1, 4-element aligned
+// rows and heads so lanes can read 4 channels with one 8/16-byte load.
+kda_status need_vec_layout(const View& v) {
+  KDA_CHECK(v.stride[v.ndim - 1] == 1, KDA_ERR_INVALID_ARG, "%s: channel axis must have stride 1", v.name);
+  for (int i = 0; i < v.ndim - 1; ++i)
+    KDA_CHECK(v.shape[i] <= 1 || v.stride[i] % 4 == 0, KDA_ERR_INVALID_ARG,
+              "%s: stride %lld on axis %d must be a multiple of 4 elements", v.name, (long long)v.stride[i], i);
+  KDA_CHECK(reinterpret_cast<uintptr_t>(v.data) % (4 * esize(v.dtype)) == 0, KDA_ERR_INVALID_ARG,
+            "%s: data must be %lld-byte aligned", v.name, (long long)(4 * esize(v.dtype)));
+  return KDA_OK;
+}
+
+// State pool [num_slots, H, 128, 128]: per-slot block contiguous, slot stride
+// >= H*128*128 and 16-byte aligned.
+kda_status need_state_layout(const View& v, int64_t H) {
+  KDA_TRY(need_dtype(v, KDA_F32, KDA_BF16));
+  KDA_CHECK(v.ndim == 4, KDA_ERR_INVALID_ARG, "state: expected rank 4");
+  KDA_TRY(need_shape(v, 1, H));
+  KDA_TRY(need_shape(v, 2, kD));
+  KDA_TRY(need_shape(v, 3, kD));
+  KDA_CHECK(v.shape[0] >= 1 && v.shape[0] <= INT32_MAX, KDA_ERR_INVALID_ARG, "state: num_slots %lld out of range",
+            (long long)v.shape[0]);
+  KDA_CHECK(v.stride[3] == 1 && v.stride[2] == kD && (H <= 1 || v.stride[1] == kUnit), KDA_ERR_INVALID_ARG,
+            "state: each slot's [H, 128, 128] block must be contiguous");
+  KDA_CHECK(v.shape[0] <= 1 || v.stride[0] >= H * kUnit, KDA_ERR_INVALID_ARG,
+            "state: slot stride %lld overlaps slots (needs >= %lld)", (long long)v.stride[0], (long long)(H * kUnit));
+  KDA_CHECK((v.stride[0] * esize(v.dtype)) % 16 == 0 || v.shape[0] <= 1, KDA_ERR_INVALID_ARG,
+            "state: slot stride must keep 16-byte alignment");
+  KDA_CHECK(reinterpret_cast<uintptr_t>(v.data) % 16 == 0, KDA_ERR_INVALID_ARG, "state: data must be 16-byte aligned");
+  return KDA_OK;
+}
+
+kda_status need_indices(const View& v, int64_t n) {
+  KDA_TRY(need_dtype(v, KDA_I32));
+  KDA_CHECK(v.ndim == 1, KDA_ERR_INVALID_ARG, "%s: expected rank 1", v.name);
+  KDA_TRY(need_shape(v, 0, n));
+  KDA_CHECK(v.shape[0] <= 1 || v.stride[0] == 1, KDA_ERR_INVALID_ARG, "%s: must be contiguous", v.name);
+  return KDA_OK;
+}
+
+kda_status need_f32_vector(const View& v, int64_t n) {
+  KDA_TRY(need_dtype(v, KDA_F32));
+  KDA_CHECK(v.numel() == n, KDA_ERR_INVALID_ARG, "%s: expected %lld elements, got %lld", v.name, (long long)n,
+            (long long)v.numel());
+  KDA_TRY(need_contiguous(v));
+  KDA_CHECK(reinterpret_cast<uintptr_t>(v.data) % 16 == 0, KDA_ERR_INVALID_ARG, "%s: data must be 16-byte aligned",
+            v.name);
+  return KDA_OK;
+}
+
+kda_status need_out(const View& v) {
+  KDA_TRY(need_dtype(v, KDA_BF16));
+  KDA_TRY(need_contiguous(v));
+  KDA_CHECK(reinterpret_cast<uintptr_t>(v.data) % 16 == 0, KDA_ERR_INVALID_ARG, "%s: data must be 16-byte aligned",
+            v.name);
+  return KDA_OK;
+}
+
+bool overlap(const View& a, const View& b) {
+  uintptr_t alo, ahi, blo, bhi;
+  a.range(&alo, &ahi);
+  b.range(&blo, &bhi);
+  if (alo == ahi || blo == bhi) return false;
+  return alo < bhi && blo < ahi;
+}
+
+// `w` is written: it must not share bytes with any other argument.
+kda_status no_alias(const View& w, std::initializer_list<const View*> others) {
+  for (const View* o : others)
+    KDA_CHECK(!overlap(w, *o), KDA_ERR_ALIAS, "%s overlaps %s", w.name, o->name);
+  return KDA_OK;
+}
+
+// ---- device properties (cached per device) ------------------------------------
+
+struct DeviceInfo {
+  int cc_major = 0, cc_minor = 0, sms = 0;
+  bool valid = false;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  KDA_CHECK(e == cudaSuccess, KDA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  KDA_CHECK(dev >= 0 && dev < 64, KDA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  {
+    std::lock_guard<std::mutex> lk(g_dev_mu);
+    if (!g_dev[dev].valid) {
+      DeviceInfo d;
+      e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+      if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+      KDA_CHECK(e == cudaSuccess, KDA_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+      d.valid = true;
+      g_dev[dev] = d;
+    }
+    *info = g_dev[dev];
+  }
+  KDA_CHECK(info->cc_major == 10 && info->cc_minor == 3, KDA_ERR_UNSUPPORTED,
+            "device %d is compute capability %d.%d; this library is built for sm_103a (GB300) only", dev,
+            info->cc_major, info->cc_minor);
+  if (stream != nullptr) {
+    int sdev = -1;
+    e = cudaStreamGetDevice(stream, &sdev);
+    KDA_CHECK(e == cudaSuccess, KDA_ERR_INVALID_ARG, "stream: %s", cudaGetErrorString(e));
+    KDA_CHECK(sdev == dev, KDA_ERR_INVALID_ARG, "stream belongs to device %d, current device is %d", sdev, dev);
+  }
+  return KDA_OK;
+}
+
+int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
+  (void)state_dtype;
+  (void)t_max;
+  const int forced = g_split_override.load();
+  if (op == KDA_OP_FUSED) return 1;
+  if (forced != 0) return forced;
+  // Smallest split whose CTA count reaches two waves of the SMs.
+  int split = 1;
+  while (split < 16 && units * split < 2LL * sms) split *= 2;
+  return split;
+}
+
+kda_status check_launch(cudaError_t e) {
+  KDA_CHECK(e == cudaSuccess, KDA_ERR_CUDA, "kernel launch: %s", cudaGetErrorString(e));
+  return KDA_OK;
+}
+
+kda_status check_grid(int64_t blocks) {
+  KDA_CHECK(blocks < (int64_t)INT32_MAX, KDA_ERR_UNSUPPORTED, "grid of %lld CTAs too large", (long long)blocks);
+  return KDA_OK;
+}
+
+kda_status check_gate(int32_t has_lower_bound, float lower_bound) {
+  KDA_CHECK(has_lower_bound == 0 || has_lower_bound == 1, KDA_ERR_INVALID_ARG, "has_lower_bound must be 0 or 1");
+  KDA_CHECK(!has_lower_bound || (std::isfinite(lower_bound) && lower_bound < 0.f), KDA_ERR_INVALID_ARG,
+            "lower_bound must be a finite negative number");
+  return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_recurrent_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                const kda_tensor* raw_gate, const kda_tensor* raw_beta, const kda_tensor* A_log,
+                                const kda_tensor* dt_bias, const kda_tensor* state_indices, const kda_tensor* state,
+                                const kda_tensor* out, int32_t has_lower_bound, float lower_bound, float scale,
+                                void* stream) {
+  View Q, K, V, G, Bt, A, DT, I, S, O;
+  KDA_TRY(ranked_view(q, "q", 3, 1, &Q));
+  KDA_TRY(ranked_view(k, "k", 3, 1, &K));
+  KDA_TRY(ranked_view(v, "v", 3, 1, &V));
+  KDA_TRY(ranked_view(raw_gate, "raw_gate", 3, 1, &G));
+  KDA_TRY(ranked_view(raw_beta, "raw_beta", 2, 1, &Bt));
+  KDA_TRY(raw_view(A_log, "A_log", &A));
+  KDA_TRY(raw_view(dt_bias, "dt_bias", &DT));
+  KDA_TRY(raw_view(state_indices, "state_indices", &I));
+  KDA_TRY(raw_view(state, "state", &S));
+  KDA_TRY(ranked_view(out, "out", 3, 1, &O));
+
+  const int64_t B = Q.shape[0], H = Q.shape[1];
+  KDA_CHECK(H >= 1, KDA_ERR_INVALID_ARG, "q: need at least one head");
+  KDA_TRY(need_dtype(Q, KDA_F32, KDA_BF16));
+  KDA_TRY(need_shape(Q, 2, kD));
+  for (View* t : {&K, &V}) {
+    KDA_CHECK(t->dtype == Q.dtype, KDA_ERR_INVALID_ARG, "%s: dtype must match q", t->name);
+    KDA_TRY(need_shape(*t, 0, B));
+    KDA_TRY(need_shape(*t, 1, H));
+    KDA_TRY(need_shape(*t, 2, kD));
+  }
+  KDA_TRY(need_dtype(G, KDA_F32, KDA_BF16));
+  KDA_TRY(need_shape(G, 0, B));
+  KDA_TRY(need_shape(G, 1, H));
+  KDA_TRY(need_shape(G, 2, kD));
+  for (View* t : {&Q, &K, &V, &G}) KDA_TRY(need_vec_layout(*t));
+  KDA_TRY(need_dtype(Bt, KDA_F32, KDA_BF16));
+  KDA_TRY(need_shape(Bt, 0, B));
+  KDA_TRY(need_shape(Bt, 1, H));
+  KDA_TRY(need_f32_vector(A, H));
+  KDA_TRY(need_f32_vector(DT, H * kD));
+  KDA_TRY(need_indices(I, B));
+  KDA_TRY(need_state_layout(S, H));
+  KDA_TRY(need_out(O));
+  KDA_TRY(need_shape(O, 0, B));
+  KDA_TRY(need_shape(O, 1, H));
+  KDA_TRY(need_shape(O, 2, kD));
+  KDA_TRY(check_gate(has_lower_bound, lower_bound));
+  KDA_CHECK(std::isfinite(scale) && scale > 0.f, KDA_ERR_INVALID_ARG, "scale must be finite and positive");
+  KDA_TRY(no_alias(O, {&Q, &K, &V, &G, &Bt, &A, &DT, &I, &S}));
+  KDA_TRY(no_alias(S, {&Q, &K, &V, &G, &Bt, &A, &DT, &I}));
+  if (B == 0) return KDA_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  KDA_TRY(current_device(st, &dev));
+  const int split = plan_split(KDA_OP_RECURRENT, B * H, S.dtype, 1, dev.sms);
+  KDA_CHECK(kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
+  KDA_TRY(check_grid(B * H * split));
+
+  kda::T1Args a{};
+  a.q = Q.data; a.k = K.data; a.v = V.data; a.gate = G.data; a.beta = Bt.data;
+  a.q_rs = Q.stride[0]; a.q_hs = Q.stride[1];
+  a.k_rs = K.stride[0]; a.k_hs = K.stride[1];
+  a.v_rs = V.stride[0]; a.v_hs = V.stride[1];
+  a.g_rs = G.stride[0]; a.g_hs = G.stride[1];
+  a.b_rs = Bt.stride[0]; a.b_hs = Bt.stride[1];
+  a.qkv_dtype = Q.dtype; a.gate_dtype = G.dtype; a.beta_dtype = Bt.dtype;
+  a.A_log = reinterpret_cast<const float*>(A.data);
+  a.dt_bias = reinterpret_cast<const float*>(DT.data);
+  a.idx = reinterpret_cast<const int32_t*>(I.data);
+  a.state = S.data; a.slot_stride = S.stride[0]; a.num_slots = (int32_t)S.shape[0];
+  a.out = O.data; a.B = (int32_t)B; a.H = (int32_t)H;
+  a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
+  a.lower_bound = lower_bound; a.scale = scale;
+  return check_launch(kda::launch_t1(a, S.dtype, split, st));
+}
+
+kda_status kda_packed_decode(const kda_tensor* mixed_qkv, const kda_tensor* raw_gate, const kda_tensor* raw_beta,
+                             const kda_tensor* A_log, const kda_tensor* dt_bias, const kda_tensor* state_indices,
+                             const kda_tensor* state, const kda_tensor* out, void* stream) {
+  constexpr int64_t H = 12, HD = H * kD;
+  View M, G, Bt, A, DT, I, S, O;
+  KDA_TRY(ranked_view(mixed_qkv, "mixed_qkv", 2, -1, &M));
+  KDA_TRY(ranked_view(raw_gate, "raw_gate", 2, -1, &G));
+  KDA_TRY(ranked_view(raw_beta, "raw_beta", 2, -1, &Bt));
+  KDA_TRY(raw_view(A_log, "A_log", &A));
+  KDA_TRY(raw_view(dt_bias, "dt_bias", &DT));
+  KDA_TRY(raw_view(state_indices, "state_indices", &I));
+  KDA_TRY(raw_view(state, "state", &S));
+  KDA_TRY(ranked_view(out, "out", 3, 1, &O));
+  const int64_t B = M.shape[0];
+  KDA_TRY(need_dtype(M, KDA_BF16));
+  KDA_TRY(need_shape(M, 1, 3 * HD));
+  KDA_TRY(need_vec_layout(M));
+  KDA_TRY(need_dtype(G, KDA_BF16));
+  KDA_TRY(need_shape(G, 0, B));
+  KDA_TRY(need_shape(G, 1, HD));
+  KDA_TRY(need_vec_layout(G));
+  KDA_TRY(need_dtype(Bt, KDA_BF16));
+  KDA_TRY(need_shape(Bt, 0, B));
+  KDA_TRY(need_shape(Bt, 1, H));
+  KDA_TRY(need_f32_vector(A, H));
+  KDA_TRY(need_f32_vector(DT, HD));
+  KDA_TRY(need_indices(I, B));
+  KDA_TRY(need_state_layout(S, H));
+  KDA_CHECK(S.dtype == KDA_BF16, KDA_ERR_INVALID_ARG, "state: the packed contract takes a bfloat16 pool");
+  KDA_TRY(need_out(O));
+  KDA_TRY(need_shape(O, 0, B));
+  KDA_TRY(need_shape(O, 1, H));
+  KDA_TRY(need_shape(O, 2, kD));
+  KDA_TRY(no_alias(O, {&M, &G, &Bt, &A, &DT, &I, &S}));
+  KDA_TRY(no_alias(S, {&M, &G, &Bt, &A, &DT, &I}));
+  if (B == 0) return KDA_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  KDA_TRY(current_device(st, &dev));
+  const int split = plan_split(KDA_OP_PACKED, B * H, S.dtype, 1, dev.sms);
+  KDA_CHECK(kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
+  KDA_TRY(check_grid(B * H * split));
+
+  kda::T1Args a{};
+  const char* m = M.data;  // bfloat16 elements: 2 bytes each
+  a.q = m; a.k = m + 2 * HD; a.v = m + 4 * HD;
+  a.q_rs = a.k_rs = a.v_rs = M.stride[0];
+  a.q_hs = a.k_hs = a.v_hs = kD;
+  a.gate = G.data; a.g_rs = G.stride[0]; a.g_hs = kD;
+  a.beta = Bt.data; a.b_rs = Bt.stride[0]; a.b_hs = Bt.stride[1];
+  a.qkv_dtype = kda::KDA_DT_BF16; a.gate_dtype = kda::KDA_DT_BF16; a.beta_dtype = kda::KDA_DT_BF16;
+  a.A_log = reinterpret_cast<const float*>(A.data);
+  a.dt_bias = reinterpret_cast<const float*>(DT.data);
+  a.idx = reinterpret_cast<const int32_t*>(I.data);
+  a.state = S.data; a.slot_stride = S.stride[0]; a.num_slots = (int32_t)S.shape[0];
+  a.out = O.data; a.B = (int32_t)B; a.H = (int32_t)H;
+  a.gate_mode = kda::KDA_GATE_LOWER_BOUND;
+  a.lower_bound = -5.0f;
+  a.scale = 0.08838834764831845f;  // 1/sqrt(128)
+  return check_launch(kda::launch_t1(a, S.dtype, split, st));
+}
+
+kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, const kda_tensor* conv_state,
+                            const kda_tensor* raw_gate, const kda_tensor* raw_beta, const kda_tensor* A_log,
+                            const kda_tensor* dt_bias, const kda_tensor* state_indices, const kda_tensor* state,
+                            const kda_tensor* output_gate, const kda_tensor* norm_weight, int32_t has_lower_bound,
+                            float lower_bound, float norm_eps, const kda_tensor* out, void* stream) {
+  View X, W, C, G, Bt, A, DT, I, S, OG, NW, O;
+  KDA_TRY(ranked_view(x, "x", 2, -1, &X));
+  KDA_TRY(raw_view(conv_weight, "conv_weight", &W));
+  KDA_TRY(ranked_view(conv_state, "conv_state", 3, -1, &C));
+  KDA_TRY(ranked_view(raw_gate, "raw_gate", 3, 0, &G));
+  KDA_TRY(ranked_view(raw_beta, "raw_beta", 2, 0, &Bt));
+  KDA_TRY(raw_view(A_log, "A_log", &A));
+  KDA_TRY(raw_view(dt_bias, "dt_bias", &DT));
+  KDA_TRY(raw_view(state_indices, "state_indices", &I));
+  KDA_TRY(raw_view(state, "state", &S));
+  KDA_TRY(ranked_view(output_gate, "output_gate", 3, 0, &OG));
+  KDA_TRY(raw_view(norm_weight, "norm_weight", &NW));
+  KDA_TRY(ranked_view(out, "out", 3, 0, &O));
+
+  KDA_CHECK(S.ndim == 4, KDA_ERR_INVALID_ARG, "state: expected rank 4");
+  const int64_t H = S.shape[1], HD = H * kD, rows = X.shape[0];
+  KDA_CHECK(H >= 1, KDA_ERR_INVALID_ARG, "state: need at least one head");
+  KDA_TRY(need_state_layout(S, H));
+  KDA_TRY(need_dtype(X, KDA_BF16));
+  KDA_TRY(need_shape(X, 1, 3 * HD));
+  KDA_CHECK(X.stride[1] == 1, KDA_ERR_INVALID_ARG, "x: channel axis must have stride 1");
+  KDA_TRY(need_dtype(W, KDA_F32));
+  KDA_CHECK(W.ndim == 3, KDA_ERR_INVALID_ARG, "conv_weight: expected rank 3");
+  KDA_TRY(need_shape(W, 0, 3));
+  KDA_TRY(need_shape(W, 1, 4));
+  KDA_TRY(need_shape(W, 2, HD));
+  KDA_TRY(need_contiguous(W));
+  KDA_TRY(need_dtype(C, KDA_BF16));
+  KDA_TRY(need_shape(C, 0, S.shape[0]));
+  KDA_TRY(need_shape(C, 1, 3 * HD));
+  KDA_TRY(need_shape(C, 2, 3));
+  KDA_CHECK(C.stride[1] == 1 && C.stride[2] == 3 * HD, KDA_ERR_INVALID_ARG,
+            "conv_state: strides must be [slot_stride, 1, 3*H*128]");
+  KDA_CHECK(C.shape[0] <= 1 || C.stride[0] >= 9 * HD, KDA_ERR_INVALID_ARG, "conv_state: slot stride overlaps slots");
+  KDA_TRY(need_dtype(G, KDA_BF16));
+  KDA_TRY(need_shape(G, 0, rows));
+  KDA_TRY(need_shape(G, 1, H));
+  KDA_TRY(need_shape(G, 2, kD));
+  KDA_CHECK(G.stride[2] == 1, KDA_ERR_INVALID_ARG, "raw_gate: channel axis must have stride 1");
+  KDA_TRY(need_dtype(Bt, KDA_BF16));
+  KDA_TRY(need_shape(Bt, 0, rows));
+  KDA_TRY(need_shape(Bt, 1, H));
+  KDA_TRY(need_f32_vector(A, H));
+  KDA_TRY(need_f32_vector(DT, HD));
+  KDA_TRY(need_indices(I, rows));
+  KDA_TRY(need_dtype(OG, KDA_BF16));
+  KDA_TRY(need_shape(OG, 0, rows));
+  KDA_TRY(need_shape(OG, 1, H));
+  KDA_TRY(need_shape(OG, 2, kD));
+  KDA_TRY(need_vec_layout(OG));
+  KDA_TRY(need_f32_vector(NW, kD));
+  KDA_TRY(need_out(O));
+  KDA_TRY(need_shape(O, 0, rows));
+  KDA_TRY(need_shape(O, 1, H));
+  KDA_TRY(need_shape(O, 2, kD));
+  KDA_TRY(check_gate(has_lower_bound, lower_bound));
+  KDA_CHECK(std::isfinite(norm_eps) && norm_eps >= 0.f, KDA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  KDA_TRY(no_alias(O, {&X, &W, &C, &G, &Bt, &A, &DT, &I, &S, &OG, &NW}));
+  KDA_TRY(no_alias(S, {&X, &W, &C, &G, &Bt, &A, &DT, &I, &OG, &NW}));
+  KDA_TRY(no_alias(C, {&X, &W, &G, &Bt, &A, &DT, &I, &OG, &NW}));
+  if (rows == 0) return KDA_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  KDA_TRY(current_device(st, &dev));
+  KDA_TRY(check_grid(rows * H));
+
+  kda::FusedArgs a{};
+  a.x = X.data; a.x_rs = X.stride[0];
+  a.conv_w = reinterpret_cast<const float*>(W.data);
+  a.conv_state = C.data; a.cs_slot_stride = C.stride[0]; a.cs_tap_stride = C.stride[2];
+  a.gate = G.data; a.g_rs = G.stride[0]; a.g_hs = G.stride[1];
+  a.beta = Bt.data; a.b_rs = Bt.stride[0]; a.b_hs = Bt.stride[1];
+  a.A_log = reinterpret_cast<const float*>(A.data);
+  a.dt_bias = reinterpret_cast<const float*>(DT.data);
+  a.idx = reinterpret_cast<const int32_t*>(I.data);
+  a.state = S.data; a.slot_stride = S.stride[0]; a.num_slots = (int32_t)S.shape[0];
+  a.out_gate = OG.data; a.og_rs = OG.stride[0]; a.og_hs = OG.stride[1];
+  a.norm_w = reinterpret_cast<const float*>(NW.data);
+  a.out = O.data; a.rows = (int32_t)rows; a.H = (int32_t)H;
+  a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
+  a.lower_bound = lower_bound; a.norm_eps = norm_eps;
+  a.scale = 0.08838834764831845f;  // 1/sqrt(128)
+  return check_launch(kda::launch_fused(a, S.dtype, st));
+}
+
+kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
+                           const kda_tensor* beta, int32_t beta_is_logit, const kda_tensor* cu_seqlens,
+                           int32_t t_max, const kda_tensor* state_indices, const kda_tensor* state,
+                           const kda_tensor* out, float scale, void* stream) {
+  View Q, K, V, Gt, Bt, CU, I, S, O;
+  KDA_TRY(ranked_view(q, "q", 3, -1, &Q));
+  KDA_TRY(ranked_view(k, "k", 3, -1, &K));
+  KDA_TRY(ranked_view(v, "v", 3, -1, &V));
+  KDA_TRY(ranked_view(g, "g", 3, -1, &Gt));
+  KDA_TRY(ranked_view(beta, "beta", 2, -1, &Bt));
+  KDA_TRY(raw_view(cu_seqlens, "cu_seqlens", &CU));
+  KDA_TRY(raw_view(state_indices, "state_indices", &I));
+  KDA_TRY(raw_view(state, "state", &S));
+  KDA_TRY(ranked_view(out, "out", 3, -1, &O));
+  const int64_t R = Q.shape[0], H = Q.shape[1];
+  KDA_CHECK(H >= 1, KDA_ERR_INVALID_ARG, "q: need at least one head");
+  KDA_CHECK(R <= INT32_MAX, KDA_ERR_INVALID_ARG, "q: too many token rows");
+  KDA_TRY(need_dtype(Q, KDA_F32, KDA_BF16));
+  KDA_TRY(need_shape(Q, 2, kD));
+  for (View* t : {&K, &V}) {
+    KDA_CHECK(t->dtype == Q.dtype, KDA_ERR_INVALID_ARG, "%s: dtype must match q", t->name);
+    KDA_TRY(need_shape(*t, 0, R));
+    KDA_TRY(need_shape(*t, 1, H));
+    KDA_TRY(need_shape(*t, 2, kD));
+  }
+  KDA_TRY(need_dtype(Gt, KDA_F32));
+  KDA_TRY(need_shape(Gt, 0, R));
+  KDA_TRY(need_shape(Gt, 1, H));
+  KDA_TRY(need_shape(Gt, 2, kD));
+  for (View* t : {&Q, &K, &V, &Gt}) KDA_TRY(need_vec_layout(*t));
+  KDA_TRY(need_dtype(Bt, KDA_F32, KDA_BF16));
+  KDA_TRY(need_shape(Bt, 0, R));
+  KDA_TRY(need_shape(Bt, 1, H));
+  KDA_CHECK(beta_is_logit == 0 || beta_is_logit == 1, KDA_ERR_INVALID_ARG, "beta_is_logit must be 0 or 1");
+  KDA_CHECK(CU.ndim == 1 && CU.shape[0] >= 1, KDA_ERR_INVALID_ARG, "cu_seqlens: expected rank 1 with N+1 >= 1 entries");
+  const int64_t N = CU.shape[0] - 1;
+  KDA_TRY(need_indices(CU, N + 1));
+  KDA_TRY(need_indices(I, N));
+  KDA_CHECK(t_max >= 1, KDA_ERR_INVALID_ARG, "t_max must be >= 1");
+  KDA_TRY(need_state_layout(S, H));
+  KDA_TRY(need_out(O));
+  KDA_TRY(need_shape(O, 0, R));
+  KDA_TRY(need_shape(O, 1, H));
+  KDA_TRY(need_shape(O, 2, kD));
+  KDA_CHECK(std::isfinite(scale) && scale > 0.f, KDA_ERR_INVALID_ARG, "scale must be finite and positive");
+  KDA_TRY(no_alias(O, {&Q, &K, &V, &Gt, &Bt, &CU, &I, &S}));
+  KDA_TRY(no_alias(S, {&Q, &K, &V, &Gt, &Bt, &CU, &I}));
+  if (R == 0) return KDA_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  KDA_TRY(current_device(st, &dev));
+  const int split = plan_split(KDA_OP_SPEC, N * H, S.dtype, t_max, dev.sms);
+  KDA_CHECK(kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
+  KDA_TRY(check_grid((N + 1) * H * split));
+
+  kda::SpecArgs a{};
+  a.q = Q.data; a.k = K.data; a.v = V.data;
+  a.q_rs = Q.stride[0]; a.q_hs = Q.stride[1];
+  a.k_rs = K.stride[0]; a.k_hs = K.stride[1];
+  a.v_rs = V.stride[0]; a.v_hs = V.stride[1];
+  a.qkv_dtype = Q.dtype;
+  a.g = reinterpret_cast<const float*>(Gt.data); a.g_rs = Gt.stride[0]; a.g_hs = Gt.stride[1];
+  a.beta = Bt.data; a.b_rs = Bt.stride[0]; a.b_hs = Bt.stride[1];
+  a.beta_dtype = Bt.dtype; a.beta_is_logit = beta_is_logit;
+  a.cu = reinterpret_cast<const int32_t*>(CU.data);
+  a.idx = reinterpret_cast<const int32_t*>(I.data);
+  a.state = S.data; a.slot_stride = S.stride[0]; a.num_slots = (int32_t)S.shape[0];
+  a.out = O.data; a.N = (int32_t)N; a.R = (int32_t)R; a.H = (int32_t)H;
+  a.scale = scale;
+  return check_launch(kda::launch_spec(a, S.dtype, split, st));
+}
+
+int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max, int32_t sm_count) {
+  if (op < KDA_OP_RECURRENT || op > KDA_OP_SPEC || units < 0 || sm_count < 1 || t_max < 1) return 0;
+  if (state_dtype != KDA_F32 && state_dtype != KDA_BF16) return 0;
+  return plan_split(op, units, state_dtype, t_max, sm_count);
+}
+
+kda_status kda_set_split_override(int32_t split) {
+  KDA_CHECK(split == 0 || kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
+  g_split_override.store(split);
+  return KDA_OK;
+}
+
+const char* kda_status_string(kda_status s) {
+  switch (s) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_ALIAS: return "KDA_ERR_ALIAS";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    default: return "KDA_ERR_UNKNOWN";
+  }
+}
+
+const char* kda_last_error_message(void) { return g_last_error.c_str(); }
+
+const char* kda_version(void) { return "libkda 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,74 @@
+// Internal interface between the host dispatcher (kda_api.cu) and the kernel
+// translation units.  Plain structs of device pointers and element strides,
+// validated on the host before any launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+enum : int { KDA_DT_F32 = 0, KDA_DT_BF16 = 1 };
+enum : int { KDA_GATE_SOFTPLUS = 0, KDA_GATE_LOWER_BOUND = 1 };
+
+// One T=1 step over B rows x H heads with split q / k / v activations
+// (the packed front end is the same with strided views into one row).
+struct T1Args {
+  const void* q; const void* k; const void* v; const void* gate; const void* beta;
+  int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs, g_rs, g_hs, b_rs, b_hs;  // element strides
+  int32_t qkv_dtype, gate_dtype, beta_dtype;
+  const float* A_log;     // [H]
+  const float* dt_bias;   // [H*128]
+  const int32_t* idx;     // [B]
+  void* state;            // [num_slots, H, 128, 128]
+  int64_t slot_stride;    // elements
+  int32_t num_slots;
+  void* out;              // bf16 [B, H, 128] contiguous
+  int32_t B, H;
+  int32_t gate_mode;
+  float lower_bound, scale;
+};
+
+// Fused conv + SiLU + KDA + gated RMSNorm, one token per row.
+struct FusedArgs {
+  const void* x; int64_t x_rs;            // bf16 [rows, 3*H*128]
+  const float* conv_w;                    // [3, 4, H*128]
+  void* conv_state;                       // bf16, [slot][tap][channel]
+  int64_t cs_slot_stride, cs_tap_stride;  // elements
+  const void* gate; int64_t g_rs, g_hs;   // bf16 [rows, H, 128]
+  const void* beta; int64_t b_rs, b_hs;   // bf16 [rows, H]
+  const float* A_log; const float* dt_bias;
+  const int32_t* idx;
+  void* state; int64_t slot_stride; int32_t num_slots;
+  const void* out_gate; int64_t og_rs, og_hs;  // bf16 [rows, H, 128]
+  const float* norm_w;                    // [128]
+  void* out;                              // bf16 [rows, H, 128]
+  int32_t rows, H;
+  int32_t gate_mode;
+  float lower_bound, norm_eps, scale;
+};
+
+// Packed speculative decode over N ragged rows of R token rows.
+struct SpecArgs {
+  const void* q; const void* k; const void* v;
+  int64_t q_rs, q_hs, k_rs, k_hs, v_rs, v_hs;
+  int32_t qkv_dtype;
+  const float* g; int64_t g_rs, g_hs;     // f32 [R, H, 128] log decay
+  const void* beta; int64_t b_rs, b_hs; int32_t beta_dtype; int32_t beta_is_logit;
+  const int32_t* cu;                      // [N+1]
+  const int32_t* idx;                     // [N]
+  void* state; int64_t slot_stride; int32_t num_slots;
+  void* out;                              // bf16 [R, H, 128]
+  int32_t N, R, H;
+  float scale;
+};
+
+// Launchers: return the launch error (cudaSuccess on success).
+cudaError_t launch_t1(const T1Args& a, int state_dtype, int split, cudaStream_t s);
+cudaError_t launch_fused(const FusedArgs& a, int state_dtype, cudaStream_t s);
+cudaError_t launch_spec(const SpecArgs& a, int state_dtype, int split, cudaStream_t s);
+
+// Splits with a compiled kernel (1, 2, 4, 8, 16).
+bool split_supported(int split);
+
+}  // namespace kda

@@ -1,0 +1,250 @@
+"""The C-ABI library: builds, loads, exports every declared symbol, and
+rejects contract breaches on the host before any CUDA call (CPU only).
+
+Descriptors here point at host memory: validation never dereferences data,
+so a breach returns its status without touching a GPU.  A call that passes
+validation on a machine without a GPU stops at the device query instead
+(KDA_ERR_CUDA or KDA_ERR_UNSUPPORTED), never at a launch.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from linear_attention_decode_02_gb300 import binding, build
+from linear_attention_decode_02_gb300.binding import KdaTensor, desc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, ALIAS, CUDA = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    with open(os.path.join(ROOT, "include", "kda.h")) as f:
+        text = f.read()
+    declared = set(re.findall(r"^(?:kda_status|int32_t|const char\*)\s+(kda_\w+)\(", text, re.M))
+    assert declared == set(binding.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kda_status_string(0) == b"KDA_OK"
+    assert lib.kda_status_string(3) == b"KDA_ERR_ALIAS"
+    assert b"sm_103a" in lib.kda_version()
+
+
+def test_plan_split_policy(lib):
+    # two waves of CTAs on 152 SMs: split doubles until units * split >= 304
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 1
+    assert binding.kda_plan_split(0, 32, 0, 1, 152) == 16
+    assert binding.kda_plan_split(2, 8, 0, 1, 152) == 1  # fused is always split 1
+    assert binding.kda_plan_split(0, 1, 5, 1, 152) == 0  # bad dtype
+    assert binding.kda_plan_split(9, 1, 0, 1, 152) == 0  # bad op
+    for units in (1, 3, 12, 100, 1000, 100000):
+        s = binding.kda_plan_split(1, units, 1, 1, 152)
+        assert s in (1, 2, 4, 8, 16)
+
+
+def test_split_override(lib):
+    assert lib.kda_set_split_override(3) == INVALID
+    assert lib.kda_set_split_override(4) == OK
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
+    assert binding.kda_plan_split(2, 16384, 0, 1, 152) == 1
+    assert lib.kda_set_split_override(0) == OK
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 1
+
+
+def _recurrent_args(B=2, H=2, N=4, qkv=torch.bfloat16, state=torch.float32):
+    t = dict(
+        q=torch.zeros(B, H, 128, dtype=qkv), k=torch.zeros(B, H, 128, dtype=qkv),
+        v=torch.zeros(B, H, 128, dtype=qkv), raw_gate=torch.zeros(B, H, 128, dtype=qkv),
+        raw_beta=torch.zeros(B, H, dtype=qkv), A_log=torch.zeros(H), dt_bias=torch.zeros(H * 128),
+        state_indices=torch.ones(B, dtype=torch.int32), state=torch.zeros(N, H, 128, 128, dtype=state),
+        out=torch.zeros(B, H, 128, dtype=torch.bfloat16))
+    return t
+
+
+def _call_recurrent(lib, t, has_lb=0, lb=0.0, scale=0.088):
+    names = ["q", "k", "v", "raw_gate", "raw_beta", "A_log", "dt_bias", "state_indices", "state", "out"]
+    ds = [desc(t[n]) if isinstance(t[n], torch.Tensor) else t[n] for n in names]
+    return lib.kda_recurrent_decode(*[ctypes.byref(d) for d in ds], has_lb, lb, scale, None)
+
+
+def _msg(lib):
+    return lib.kda_last_error_message().decode()
+
+
+def test_recurrent_valid_args_reach_the_device_query(lib):
+    st = _call_recurrent(lib, _recurrent_args())
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: the call would launch")
+    assert st in (CUDA, UNSUPPORTED), _msg(lib)
+
+
+@pytest.mark.parametrize("mutate,expect,text", [
+    (lambda t: t.update(q=torch.zeros(2, 2, 64, dtype=torch.bfloat16)), INVALID, "q: axis 2"),
+    (lambda t: t.update(k=torch.zeros(2, 2, 128, dtype=torch.float32)), INVALID, "dtype must match q"),
+    (lambda t: t.update(state_indices=torch.ones(2, dtype=torch.float32)), INVALID, "state_indices: dtype"),
+    (lambda t: t.update(state=torch.zeros(4, 3, 128, 128)), INVALID, "state: axis 1"),
+    (lambda t: t.update(state=torch.zeros(4, 2, 128, 128, dtype=torch.int32)), INVALID, "state: dtype"),
+    (lambda t: t.update(state=torch.zeros(4, 2, 128, 256)[..., :128]), INVALID, "contiguous"),
+    (lambda t: t.update(out=torch.zeros(2, 2, 128, dtype=torch.float32)), INVALID, "out: dtype"),
+    (lambda t: t.update(out=torch.zeros(2, 128, 2, dtype=torch.bfloat16).transpose(1, 2)), INVALID, "contiguous"),
+    (lambda t: t.update(q=torch.zeros(2, 2, 130, dtype=torch.bfloat16)[..., 1:129]), INVALID, "multiple of 4"),
+    (lambda t: t.update(q=torch.zeros(2, 2, 132, dtype=torch.bfloat16)[..., 2:130]), INVALID, "aligned"),
+    (lambda t: t.update(A_log=torch.zeros(3)), INVALID, "A_log"),
+    (lambda t: t.update(dt_bias=torch.zeros(2 * 64)), INVALID, "dt_bias"),
+    (lambda t: t.update(raw_beta=torch.zeros(2, 3, dtype=torch.bfloat16)), INVALID, "raw_beta"),
+])
+def test_recurrent_rejects_breaches(lib, mutate, expect, text):
+    t = _recurrent_args()
+    mutate(t)
+    assert _call_recurrent(lib, t) == expect
+    assert text in _msg(lib)
+
+
+def test_recurrent_rejects_aliasing_out_and_state(lib):
+    t = _recurrent_args()
+    t["out"] = t["state"].view(-1)[: 2 * 2 * 128].view(torch.bfloat16)[: 2 * 2 * 128].view(2, 2, 128)
+    assert _call_recurrent(lib, t) == ALIAS
+    assert "overlaps" in _msg(lib)
+    t = _recurrent_args()
+    t["state"] = torch.zeros(4, 2, 128, 128)
+    t["q"] = t["state"].view(torch.bfloat16).view(-1)[: 2 * 2 * 128].view(2, 2, 128)
+    assert _call_recurrent(lib, t) == ALIAS
+
+
+def test_recurrent_rejects_bad_gate_and_scale(lib):
+    assert _call_recurrent(lib, _recurrent_args(), has_lb=1, lb=1.0) == INVALID
+    assert _call_recurrent(lib, _recurrent_args(), has_lb=2, lb=-5.0) == INVALID
+    assert _call_recurrent(lib, _recurrent_args(), scale=0.0) == INVALID
+    assert _call_recurrent(lib, _recurrent_args(), scale=float("nan")) == INVALID
+
+
+def test_null_descriptor_is_rejected(lib):
+    t = _recurrent_args()
+    names = ["q", "k", "v", "raw_gate", "raw_beta", "A_log", "dt_bias", "state_indices", "state", "out"]
+    ptrs = [ctypes.byref(desc(t[n])) for n in names]
+    ptrs[4] = None
+    assert lib.kda_recurrent_decode(*ptrs, 0, 0.0, 0.088, None) == INVALID
+    assert "raw_beta: null" in _msg(lib)
+
+
+def test_empty_batch_launches_nothing(lib):
+    t = _recurrent_args(B=0)
+    assert _call_recurrent(lib, t) == OK
+
+
+def _packed_args(B=3, N=4):
+    return dict(mixed_qkv=torch.zeros(B, 4608, dtype=torch.bfloat16),
+                raw_gate=torch.zeros(B, 1536, dtype=torch.bfloat16),
+                raw_beta=torch.zeros(B, 12, dtype=torch.bfloat16), A_log=torch.zeros(12),
+                dt_bias=torch.zeros(1536), state_indices=torch.ones(B, dtype=torch.int32),
+                state=torch.zeros(N, 12, 128, 128, dtype=torch.bfloat16),
+                out=torch.zeros(B, 1, 12, 128, dtype=torch.bfloat16))
+
+
+def _call_packed(lib, t):
+    names = ["mixed_qkv", "raw_gate", "raw_beta", "A_log", "dt_bias", "state_indices", "state", "out"]
+    return lib.kda_packed_decode(*[ctypes.byref(desc(t[n])) for n in names], None)
+
+
+def test_packed_contract(lib):
+    st = _call_packed(lib, _packed_args())
+    assert st in (CUDA, UNSUPPORTED, OK)
+    for key, val, text in [
+        ("mixed_qkv", torch.zeros(3, 4096, dtype=torch.bfloat16), "mixed_qkv: axis 1"),
+        ("state", torch.zeros(4, 12, 128, 128), "bfloat16 pool"),
+        ("raw_gate", torch.zeros(3, 1536), "raw_gate: dtype"),
+        ("out", torch.zeros(3, 1, 8, 128, dtype=torch.bfloat16), "out: axis 1"),
+    ]:
+        t = _packed_args()
+        t[key] = val
+        assert _call_packed(lib, t) == INVALID
+        assert text in _msg(lib)
+    # a padded packed row (row stride > 4608) is accepted by validation
+    t = _packed_args()
+    t["mixed_qkv"] = torch.zeros(3, 4608 + 64, dtype=torch.bfloat16)[:, :4608]
+    assert _call_packed(lib, t) in (CUDA, UNSUPPORTED, OK)
+
+
+def _fused_args(H=8, rows=4, N=9, state=torch.float32):
+    HD = H * 128
+    return dict(x=torch.zeros(rows, 3 * HD, dtype=torch.bfloat16), conv_weight=torch.zeros(3, 4, HD),
+                conv_state=torch.zeros(N, 3, 3 * HD, dtype=torch.bfloat16).permute(0, 2, 1),
+                raw_gate=torch.zeros(1, rows, H, 128, dtype=torch.bfloat16),
+                raw_beta=torch.zeros(1, rows, H, dtype=torch.bfloat16), A_log=torch.zeros(H),
+                dt_bias=torch.zeros(HD), state_indices=torch.ones(rows, dtype=torch.int32),
+                state=torch.zeros(N, H, 128, 128, dtype=state),
+                output_gate=torch.zeros(rows, H, 128, dtype=torch.bfloat16), norm_weight=torch.ones(128),
+                out=torch.zeros(1, rows, H, 128, dtype=torch.bfloat16))
+
+
+def _call_fused(lib, t, has_lb=1, lb=-5.0, eps=1e-5):
+    names = ["x", "conv_weight", "conv_state", "raw_gate", "raw_beta", "A_log", "dt_bias",
+             "state_indices", "state", "output_gate", "norm_weight"]
+    ds = [ctypes.byref(desc(t[n])) for n in names]
+    return lib.kda_fused_decode(*ds, has_lb, lb, eps, ctypes.byref(desc(t["out"])), None)
+
+
+def test_fused_contract(lib):
+    assert _call_fused(lib, _fused_args()) in (CUDA, UNSUPPORTED, OK)
+    t = _fused_args()
+    t["conv_state"] = torch.zeros(9, 3 * 1024, 3, dtype=torch.bfloat16)  # tap-contiguous layout
+    assert _call_fused(lib, t) == INVALID
+    assert "conv_state: strides" in _msg(lib)
+    t = _fused_args()
+    t["conv_state"] = torch.zeros(5, 3, 3 * 1024, dtype=torch.bfloat16).permute(0, 2, 1)
+    assert _call_fused(lib, t) == INVALID  # num_slots differ
+    t = _fused_args()
+    t["norm_weight"] = torch.ones(64)
+    assert _call_fused(lib, t) == INVALID
+    assert _call_fused(lib, _fused_args(), eps=-1.0) == INVALID
+    t = _fused_args()
+    t["out"] = t["x"].view(-1)[: 4 * 8 * 128].view(1, 4, 8, 128)
+    assert _call_fused(lib, t) == ALIAS
+    t = _fused_args()
+    buf = torch.zeros(9 * 3 * 3 * 1024, dtype=torch.bfloat16)
+    t["x"] = buf[: 4 * 3 * 1024].view(4, 3 * 1024)
+    t["conv_state"] = buf.view(9, 3, 3 * 1024).permute(0, 2, 1)
+    assert _call_fused(lib, t) == ALIAS
+    assert "conv_state overlaps x" in _msg(lib)
+
+
+def _spec_args(R=7, N=3, H=2, M=12):
+    return dict(q=torch.zeros(R, H, 128, dtype=torch.bfloat16), k=torch.zeros(R, H, 128, dtype=torch.bfloat16),
+                v=torch.zeros(R, H, 128, dtype=torch.bfloat16), g=torch.zeros(R, H, 128),
+                beta=torch.zeros(R, H, dtype=torch.bfloat16),
+                cu_seqlens=torch.tensor([0, 2, 5, 7], dtype=torch.int32)[: N + 1],
+                state_indices=torch.ones(N, dtype=torch.int32), state=torch.zeros(M, H, 128, 128),
+                out=torch.zeros(R, H, 128, dtype=torch.bfloat16))
+
+
+def _call_spec(lib, t, t_max=3, logit=1, scale=0.088):
+    d = {n: ctypes.byref(desc(v)) for n, v in t.items()}
+    return lib.kda_spec_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], logit, d["cu_seqlens"], t_max,
+                               d["state_indices"], d["state"], d["out"], scale, None)
+
+
+def test_spec_contract(lib):
+    assert _call_spec(lib, _spec_args()) in (CUDA, UNSUPPORTED, OK)
+    t = _spec_args()
+    t["g"] = torch.zeros(7, 2, 128, dtype=torch.bfloat16)
+    assert _call_spec(lib, t) == INVALID
+    t = _spec_args()
+    t["state_indices"] = torch.ones(4, dtype=torch.int32)
+    assert _call_spec(lib, t) == INVALID
+    assert _call_spec(lib, _spec_args(), t_max=0) == INVALID
+    assert _call_spec(lib, _spec_args(), logit=3) == INVALID
+    t = _spec_args(R=0)
+    t["cu_seqlens"] = torch.zeros(4, dtype=torch.int32)
+    assert _call_spec(lib, t) == OK  # no token rows: nothing to launch
