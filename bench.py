@@ -1,20 +1,23 @@
 """Benchmark of the KDA decode hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload recurrent|packed|fused|spec] [--batch B] [--heads H]
+                    [--slots S] [--t-max T] [--no-paths] [--no-e2e] [--cpu-seconds X]
 
-Headline workload: Kimi-Linear equal-head T=1 recurrent decode, H=32,
-K=V=128, float32 state pool [1024, 32, 128, 128], B=512 rows on distinct
-slots, bf16 activations, softplus gate.  A step is one kda_recurrent_decode
-call; two disjoint slot sets alternate between steps and every step moves
-1.07 GB of state, far more than the 129 MB L2, so no flush is needed there.
+Default (headline) workload: Kimi-Linear equal-head T=1 recurrent decode,
+H=32, K=V=128, float32 state pool [1024, 32, 128, 128], B=512 rows on
+distinct slots, bf16 activations, softplus gate.  A step is one
+kda_recurrent_decode call; two random slot sets alternate between steps and
+every step moves 1.07 GB of state, far more than the 129 MB L2.
 
 Metric: achieved HBM GB/s of the algorithmic bytes (live state read + write
 plus the activations and parameters read and the output written) per call;
 ms_per_step is the time per call.  The line also carries the same metric end
 to end (pinned host inputs copied in and the output copied out each step),
 the roofline of the kernel against the measured copy bandwidth, the SM clocks
-seen during the timed region, per-path / per-batch measurements of the four
-entry points, and the float64 oracle timed on the host cores.
+seen during the timed region, per-path / per-batch CUDA-graph measurements of
+the four entry points (L2 flushed between replays), and the float64 oracle
+timed on the host cores.
 
 Multi-GPU: every rank runs its own replica (the decode units are independent
 and need no exchange); value sums the bytes of all ranks over the slowest
@@ -38,7 +41,6 @@ os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
 os.environ.setdefault("OMP_NUM_THREADS", "1")
 os.environ.setdefault("MKL_NUM_THREADS", "1")
 
-import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -48,9 +50,8 @@ from linear_attention_decode_02_gb300 import binding, synth  # noqa: E402
 
 D = 128
 METRIC = "KDA decode µs/call and achieved HBM GB/s (state R+W) vs GB300 peak, 1 GPU"
-HEADLINE = dict(workload="kimi_linear_t1_recurrent", H=32, B=512, num_slots=1024, state="float32",
-                activations="bfloat16", gate="softplus")
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
 
 
 # ---- byte model (algorithmic bytes per call) -------------------------------------
@@ -75,6 +76,151 @@ def bytes_spec(tokens_live, rows_live, rows, R, H, state_esize):
     zero_tok = R - tokens_live
     return (rows_live * H * 2 * D * D * state_esize + tokens_live * H * per_tok + zero_tok * H * 2 * D
             + (rows + 1) * 4 + rows * 4)
+
+
+# ---- workloads ---------------------------------------------------------------------
+
+def _device_pool(num_slots, H, dtype, seed):
+    gen = torch.Generator(device="cuda").manual_seed(seed)
+    pool = torch.empty(num_slots, H, D, D, dtype=torch.float32, device="cuda").normal_(0.0, 0.1, generator=gen)
+    return pool if dtype == torch.float32 else pool.to(dtype)
+
+
+def _slot_sets(n_sets, count, num_slots, null_count, seed, null_values=(-1,)):
+    g = torch.Generator().manual_seed(seed + 7)
+    sets = []
+    for _ in range(n_sets):
+        s = synth.with_nulls(g, synth.distinct_slots(g, count, num_slots), null_count, null_values)
+        sets.append(s)
+    return sets
+
+
+class Workload:
+    """One decode path at one size: device inputs, a call per step, its byte model."""
+
+    name = ""
+
+    def call(self, idx):
+        raise NotImplementedError
+
+    def step(self, i):
+        self.call(self.sets[i % len(self.sets)])
+
+    def e2e_step(self, i, host, dev_idx):
+        for k, t in host.items():
+            if k != "idx":
+                self.d[k].copy_(t, non_blocking=True)
+        dev_idx.copy_(host["idx"][i % len(host["idx"])], non_blocking=True)
+        self.call(dev_idx)
+        self.out_h.copy_(self.out, non_blocking=True)
+
+
+class Recurrent(Workload):
+    def __init__(self, B=512, H=32, slots=1024, state_dtype=torch.float32, n_sets=2, null_count=0, seed=0,
+                 lower_bound=None):
+        self.name = f"recurrent_h{H}_{'f32' if state_dtype == torch.float32 else 'bf16'}_b{B}"
+        c = synth.recurrent_case(B, H, slots, seed=seed, make_state=False)
+        self.d = {k: v.cuda() for k, v in c.items() if k not in ("state", "state_indices")}
+        self.d["state"] = _device_pool(slots, H, state_dtype, seed)
+        self.sets = [s.cuda() for s in _slot_sets(n_sets, B, slots, null_count, seed)]
+        self.out = torch.empty(B, H, D, dtype=torch.bfloat16, device="cuda")
+        self.lower_bound = lower_bound
+        esz = 4 if state_dtype == torch.float32 else 2
+        self.nbytes = bytes_t1(B - null_count, null_count, H, esz)
+        self.config = dict(workload="kimi_linear_t1_recurrent", H=H, B=B, num_slots=slots,
+                           state="float32" if esz == 4 else "bfloat16", activations="bfloat16",
+                           gate="softplus" if lower_bound is None else f"lower_bound {lower_bound}")
+        self.e2e_keys = ("q", "k", "v", "raw_gate", "raw_beta")
+
+    def call(self, idx):
+        d = self.d
+        binding.kda_recurrent_decode(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["A_log"], d["dt_bias"],
+                                     idx, d["state"], out=self.out, lower_bound=self.lower_bound)
+
+
+class Packed(Workload):
+    def __init__(self, B=512, slots=2048, n_sets=2, null_frac=0.1, seed=0):
+        self.name = f"packed_k3_bf16_b{B}"
+        nn = int(math.floor(null_frac * B))
+        c = synth.packed_case(B, num_slots=slots, seed=seed, null_frac=0.0, make_state=False)
+        self.d = {k: v.cuda() for k, v in c.items() if k not in ("state", "state_indices")}
+        self.d["state"] = _device_pool(slots, 12, torch.bfloat16, seed)
+        self.sets = [s.cuda() for s in _slot_sets(n_sets, B, slots, nn, seed)]
+        self.out = torch.empty(B, 1, 12, D, dtype=torch.bfloat16, device="cuda")
+        self.nbytes = bytes_t1(B - nn, nn, 12, 2)
+        self.config = dict(workload="packed_kimi_k3_t1", H=12, B=B, num_slots=slots, state="bfloat16",
+                           padding_rows=nn, gate="lower_bound -5")
+        self.e2e_keys = ("mixed_qkv", "raw_gate", "raw_beta")
+
+    def call(self, idx):
+        d = self.d
+        binding.kda_packed_decode(d["mixed_qkv"], d["raw_gate"], d["raw_beta"], d["A_log"], d["dt_bias"], idx,
+                                  d["state"], out=self.out)
+
+
+class Fused(Workload):
+    def __init__(self, H=32, rows=256, slots=None, state_dtype=torch.float32, n_sets=2, null_frac=0.1, seed=0,
+                 lower_bound=-5.0):
+        slots = slots or 2 * rows + 1
+        self.name = f"fused_h{H}_rows{rows}_{'f32' if state_dtype == torch.float32 else 'bf16'}"
+        nn = int(math.floor(null_frac * rows))
+        c = synth.fused_case(H, rows, seed=seed, num_slots=slots, null_frac=0.0, make_state=False)
+        self.d = {k: v.cuda() for k, v in c.items() if k not in ("state", "state_indices", "conv_state")}
+        self.d["state"] = _device_pool(slots, H, state_dtype, seed)
+        gen = torch.Generator(device="cuda").manual_seed(seed + 1)
+        phys = torch.empty(slots, 3, 3 * H * D, dtype=torch.float32, device="cuda").normal_(generator=gen)
+        self.d["conv_state"] = phys.to(torch.bfloat16).permute(0, 2, 1)
+        self.sets = [s.cuda() for s in _slot_sets(n_sets, rows, slots, nn, seed, (0, -1))]
+        self.out = torch.empty(1, rows, H, D, dtype=torch.bfloat16, device="cuda")
+        self.lower_bound = lower_bound
+        self.nbytes = bytes_fused(rows - nn, nn, H, 4 if state_dtype == torch.float32 else 2)
+        self.config = dict(workload="fused_conv_kda_gated_rmsnorm_t1", H=H, rows=rows, num_slots=slots,
+                           state="float32" if state_dtype == torch.float32 else "bfloat16", null_rows=nn,
+                           gate=f"lower_bound {lower_bound}" if lower_bound is not None else "softplus")
+        self.e2e_keys = ("x", "raw_gate", "raw_beta", "output_gate")
+
+    def call(self, idx):
+        d = self.d
+        binding.kda_fused_decode(d["x"], d["conv_weight"], d["conv_state"], d["raw_gate"], d["raw_beta"], d["A_log"],
+                                 d["dt_bias"], idx, d["state"], d["output_gate"], d["norm_weight"],
+                                 lower_bound=self.lower_bound, out=self.out)
+
+
+class Spec(Workload):
+    def __init__(self, N=128, t_max=6, H=16, slots=None, state_dtype=torch.float32, n_sets=2, seed=0):
+        slots = slots or 4 * N
+        self.name = f"spec_h{H}_n{N}_t{t_max}_{'f32' if state_dtype == torch.float32 else 'bf16'}"
+        c = synth.spec_case(N, t_max, seed=seed, H=H, num_slots=slots, make_state=False)
+        self.t_max = t_max
+        self.d = {k: v.cuda() for k, v in c.items() if isinstance(v, torch.Tensor) and k not in ("state",
+                                                                                                   "state_indices")}
+        self.d["state"] = _device_pool(slots, H, state_dtype, seed)
+        self.sets = [s.cuda() for s in _slot_sets(n_sets, N, slots, 0, seed)]
+        R = c["q"].shape[0]
+        self.out = torch.empty(R, H, D, dtype=torch.bfloat16, device="cuda")
+        lens = c["lengths"]
+        live_rows = int((lens > 0).sum())
+        self.nbytes = bytes_spec(R, live_rows, N, R, H, 4 if state_dtype == torch.float32 else 2)
+        self.config = dict(workload="packed_speculative_ragged", H=H, rows=N, t_max=t_max, tokens=R,
+                           empty_rows=N - live_rows, num_slots=slots,
+                           state="float32" if state_dtype == torch.float32 else "bfloat16",
+                           gates="precomputed fp32 log decay in [-5, 0]")
+        self.e2e_keys = ("q", "k", "v", "g", "beta", "cu_seqlens")
+
+    def call(self, idx):
+        d = self.d
+        binding.kda_spec_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], d["cu_seqlens"], idx, d["state"],
+                                self.t_max, out=self.out)
+
+
+def make_workload(args, seed):
+    if args.workload == "recurrent":
+        return Recurrent(B=args.batch or 512, H=args.heads or 32, slots=args.slots or 1024, seed=seed)
+    if args.workload == "packed":
+        return Packed(B=args.batch or 512, slots=args.slots or 2048, seed=seed)
+    if args.workload == "fused":
+        return Fused(H=args.heads or 32, rows=args.batch or 256, slots=args.slots, seed=seed)
+    return Spec(N=args.batch or 128, t_max=args.t_max or 6, H=args.heads or 16, slots=args.slots, seed=seed)
 
 
 # ---- environment -------------------------------------------------------------------
@@ -107,17 +253,16 @@ def ncu_traffic(kind):
     if rec.get("source_hash") != kernel_source_hash():
         return None
     entry = rec.get("kernels", {}).get(kind)
-    if not entry:
-        return None
-    return entry.get("dram_bytes_per_launch")
+    return entry.get("dram_bytes_per_launch") if entry else None
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms while running."""
+    """nvidia-smi SM clocks and throttle reasons sampled every 100 ms while running."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index=0):
         self.samples = []
@@ -141,8 +286,7 @@ class ClockSampler:
         except OSError:
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
+        threading.Thread(target=self._read, daemon=True).start()
         time.sleep(0.3)
 
     def _read(self):
@@ -160,21 +304,28 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self, t0, t1):
-        rows = [p for (t, p) in self.samples if t0 <= t <= t1] or [p for (_, p) in self.samples]
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        rows = inside or [p for (_, p) in self.samples]
         if not rows:
             return None
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        sm = [float(p[0]) for p in rows if p[0].replace(".", "").isdigit()]
-        mx = [float(p[1]) for p in rows if p[1].replace(".", "").isdigit()]
-        reasons = sorted({names[i] for p in rows for i in range(4) if p[3 + i].lower().startswith("active")})
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [v for v in (num(p[0]) for p in rows) if v is not None]
+        mx = [v for v in (num(p[1]) for p in rows) if v is not None]
+        reasons = sorted({self.REASONS[i] for p in rows for i in range(4) if p[3 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
 # ---- timing helpers ------------------------------------------------------------------
 
-def time_direct(fn, steps, warmup, stream, barrier):
-    """Average ms per call over `steps` back-to-back launches on `stream`."""
+def time_direct(fn, steps, warmup, barrier):
+    """Average ms per step over `steps` back-to-back steps on the current stream."""
+    stream = torch.cuda.current_stream()
     for i in range(warmup):
         fn(i)
     barrier()
@@ -191,166 +342,70 @@ def time_direct(fn, steps, warmup, stream, barrier):
     return e0.elapsed_time(e1) / steps, (wall0, wall1)
 
 
-def time_graph(calls, reps, flush):
-    """Per-call ms of a CUDA graph of `calls` launches, L2 flushed before each replay."""
+def time_graph(wl, n_calls, reps, flush):
+    """Per-call ms of a CUDA graph of `n_calls` launches on rotating slot sets, L2 flushed before each replay."""
     g = torch.cuda.CUDAGraph()
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        for fn in calls:
-            fn()
+        for i in range(n_calls):
+            wl.step(i)
     torch.cuda.current_stream().wait_stream(s)
     with torch.cuda.graph(g):
-        for fn in calls:
-            fn()
+        for i in range(n_calls):
+            wl.step(i)
     times = []
     for r in range(reps + 2):
-        flush.fill_(r)
+        flush.fill_(float(r))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         g.replay()
         e1.record()
         torch.cuda.synchronize()
         if r >= 2:
-            times.append(e0.elapsed_time(e1) / len(calls))
+            times.append(e0.elapsed_time(e1) / n_calls)
     return statistics.median(times)
 
 
-# ---- workloads -------------------------------------------------------------------------
-
-def recurrent_device_case(B, H, num_slots, seed, state_dtype=torch.float32, null_count=0, n_sets=2):
-    """Device inputs with `n_sets` disjoint slot sets (alternated between steps)."""
-    g = torch.Generator().manual_seed(seed)
-    case = synth.recurrent_case(B, H, 2, seed=seed, state_dtype=state_dtype, state_indices=[1] * B)
-    d = {k: v.cuda() for k, v in case.items() if k not in ("state", "state_indices")}
-    perm = (torch.randperm(num_slots - 1, generator=g) + 1).to(torch.int32)
-    sets = []
-    for i in range(n_sets):
-        idx = perm[i * B:(i + 1) * B].clone()
-        if null_count:
-            idx = synth.with_nulls(g, idx, null_count)
-        sets.append(idx.cuda())
-    gen = torch.Generator(device="cuda").manual_seed(seed)
-    state = torch.empty(num_slots, H, D, D, dtype=torch.float32, device="cuda")
-    state.normal_(0.0, 0.1, generator=gen)
-    d["state"] = state.to(state_dtype) if state_dtype != torch.float32 else state
-    d["sets"] = sets
-    return d
-
-
-def run_recurrent(d, i, out):
-    binding.kda_recurrent_decode(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["A_log"], d["dt_bias"],
-                                 d["sets"][i % len(d["sets"])], d["state"], out=out)
-
-
-def headline(args, rank, world, barrier, peaks):
-    H, B, N = HEADLINE["H"], HEADLINE["B"], HEADLINE["num_slots"]
-    d = recurrent_device_case(B, H, N, seed=rank)
-    out = torch.empty(B, H, D, dtype=torch.bfloat16, device="cuda")
-    stream = torch.cuda.current_stream()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
-    ms, (w0, w1) = time_direct(lambda i: run_recurrent(d, i, out), args.steps, args.warmup, stream, barrier)
-    clocks.stop()
-    nbytes = bytes_t1(B, 0, H, 4)
-    return ms, nbytes, clocks.summary(w0, w1), d, out
-
-
-def e2e_recurrent(d, steps, warmup, barrier):
-    """Same call with pinned-host activations copied in and the output copied out every step."""
-    host = {k: d[k].cpu().pin_memory() for k in ("q", "k", "v", "raw_gate", "raw_beta")}
-    host["sets"] = [s.cpu().pin_memory() for s in d["sets"]]
-    out = torch.empty(d["q"].shape, dtype=torch.bfloat16, device="cuda")
-    out_h = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    idx = torch.empty_like(d["sets"][0])
-
-    def step(i):
-        for k in ("q", "k", "v", "raw_gate", "raw_beta"):
-            d[k].copy_(host[k], non_blocking=True)
-        idx.copy_(host["sets"][i % len(host["sets"])], non_blocking=True)
-        binding.kda_recurrent_decode(d["q"], d["k"], d["v"], d["raw_gate"], d["raw_beta"], d["A_log"],
-                                     d["dt_bias"], idx, d["state"], out=out)
-        out_h.copy_(out, non_blocking=True)
-
-    ms, _ = time_direct(step, steps, warmup, torch.cuda.current_stream(), barrier)
-    h2d = sum(host[k].numel() * host[k].element_size() for k in ("q", "k", "v", "raw_gate", "raw_beta"))
-    h2d += host["sets"][0].numel() * 4
-    d2h = out_h.numel() * out_h.element_size()
+def e2e(wl, steps, warmup, barrier):
+    """The same call with pinned-host activations and indices copied in, the output copied out."""
+    host = {k: wl.d[k].cpu().pin_memory() for k in wl.e2e_keys}
+    host["idx"] = [s.cpu().pin_memory() for s in wl.sets]
+    wl.out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+    dev_idx = torch.empty_like(wl.sets[0])
+    ms, _ = time_direct(lambda i: wl.e2e_step(i, host, dev_idx), steps, warmup, barrier)
+    h2d = sum(host[k].numel() * host[k].element_size() for k in wl.e2e_keys) + host["idx"][0].numel() * 4
+    d2h = wl.out_h.numel() * wl.out_h.element_size()
     return ms, h2d, d2h
 
 
 def path_measurements(flush, peak):
-    """Per-path and per-batch CUDA-graph timings (L2 flushed before each replay)."""
+    """CUDA-graph timings of the four entry points over their configured sizes."""
     res = {}
 
-    def rec(name, ms, nbytes, extra=None):
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        res[name] = dict(us=round(ms * 1e3, 3), gbs=round(gbs, 1), frac=round(gbs / peak, 4), **(extra or {}))
+    def run(wl, n_sets):
+        ms = time_graph(wl, n_sets, 10, flush)
+        gbs = wl.nbytes / (ms * 1e-3) / 1e9
+        res[wl.name] = dict(us=round(ms * 1e3, 3), gbs=round(gbs, 1), frac=round(gbs / peak, 4))
 
-    # Kimi-Linear recurrent, batch sweep (20 calls per graph on disjoint slot sets)
     for B in (1, 8, 32, 128, 512):
-        n_sets = max(1, min(20, 1023 // B))
-        d = recurrent_device_case(B, 32, 1024, seed=B, n_sets=n_sets)
-        out = torch.empty(B, 32, D, dtype=torch.bfloat16, device="cuda")
-        calls = [(lambda i=i: run_recurrent(d, i, out)) for i in range(n_sets if B < 512 else 2)]
-        rec(f"recurrent_h32_f32_b{B}", time_graph(calls, 10, flush), bytes_t1(B, 0, 32, 4))
-        del d
-    # packed Kimi K3 (bf16 state, 10% padding rows), B sweep
-    for B in (1, 8, 32, 128, 512):
-        nn = int(math.floor(0.1 * B))
-        n_sets = max(1, min(20, 2047 // B))
-        g = torch.Generator().manual_seed(B)
-        c = synth.packed_case(B, num_slots=2, seed=B, null_frac=0.0)
-        c["state_indices"] = torch.ones(B, dtype=torch.int32)
-        dd = {k: v.cuda() for k, v in c.items() if k != "state"}
-        perm = (torch.randperm(2047, generator=g) + 1).to(torch.int32)
-        sets = [synth.with_nulls(g, perm[i * B:(i + 1) * B].clone(), nn).cuda() for i in range(n_sets)]
-        gen = torch.Generator(device="cuda").manual_seed(B)
-        state = torch.empty(2048, 12, D, D, dtype=torch.float32, device="cuda").normal_(0, 0.1, generator=gen)
-        state = state.to(torch.bfloat16)
-        out = torch.empty(B, 1, 12, D, dtype=torch.bfloat16, device="cuda")
-
-        def pk(i, dd=dd, sets=sets, state=state, out=out):
-            binding.kda_packed_decode(dd["mixed_qkv"], dd["raw_gate"], dd["raw_beta"], dd["A_log"], dd["dt_bias"],
-                                      sets[i], state, out=out)
-        calls = [(lambda i=i: pk(i)) for i in range(n_sets)]
-        rec(f"packed_k3_bf16_b{B}", time_graph(calls, 10, flush), bytes_t1(B - nn, nn, 12, 2))
-        del state
-    # fused conv + KDA + gated RMSNorm, fp32 state, 10% null rows
-    for H, rows in ((8, 256), (32, 256), (96, 256), (32, 32)):
-        c = synth.fused_case(H, rows, seed=H, num_slots=2 * rows + 1)
-        nn = int((c["state_indices"] <= 0).sum())
-        dd = {k: v.cuda() for k, v in c.items() if k != "conv_state"}
-        dd["conv_state"] = c["conv_state"].permute(0, 2, 1).contiguous().cuda().permute(0, 2, 1)
-        out = torch.empty(1, rows, H, D, dtype=torch.bfloat16, device="cuda")
-
-        def fz(dd=dd, out=out):
-            binding.kda_fused_decode(dd["x"], dd["conv_weight"], dd["conv_state"], dd["raw_gate"], dd["raw_beta"],
-                                     dd["A_log"], dd["dt_bias"], dd["state_indices"], dd["state"],
-                                     dd["output_gate"], dd["norm_weight"], out=out)
-        rec(f"fused_h{H}_rows{rows}_f32", time_graph([fz], 10, flush), bytes_fused(rows - nn, nn, H, 4))
-        del dd
-    # speculative ragged rows, H=16, fp32 pool [4N]
-    for N, T in ((128, 2), (128, 6), (16, 6)):
-        c = synth.spec_case(N, T, seed=N + T)
-        dd = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
-        out = torch.empty(c["q"].shape, dtype=torch.bfloat16, device="cuda")
-        lens = c["lengths"]
-        live_rows = int((lens > 0).sum())
-
-        def sp(dd=dd, out=out, T=T):
-            binding.kda_spec_decode(dd["q"], dd["k"], dd["v"], dd["g"], dd["beta"], dd["cu_seqlens"],
-                                    dd["state_indices"], dd["state"], T, out=out)
-        R = c["q"].shape[0]
-        rec(f"spec_h16_n{N}_t{T}_f32", time_graph([sp], 10, flush),
-            bytes_spec(R, live_rows, N, R, 16, 4), {"tokens": R})
-        del dd
+        n = max(1, min(16, 1023 // B))
+        run(Recurrent(B=B, H=32, slots=1024, n_sets=n, seed=B), n)
+    for B in (1, 8, 16, 31, 32, 64, 128, 256, 512):
+        n = max(1, min(16, 2047 // B))
+        run(Packed(B=B, slots=2048, n_sets=n, seed=B), n)
+    for H, rows in ((8, 1), (8, 32), (8, 256), (12, 256), (32, 32), (32, 256), (96, 256)):
+        n = max(1, min(16, (2 * rows) // max(rows, 1)))
+        run(Fused(H=H, rows=rows, n_sets=n, seed=H + rows), n)
+    for N, T in ((1, 6), (16, 6), (128, 2), (128, 4), (128, 6)):
+        run(Spec(N=N, t_max=T, H=16, n_sets=2, seed=N + T), 2)
+    torch.cuda.empty_cache()
     return res
 
 
 # ---- CPU oracle -------------------------------------------------------------------------
 
-def oracle_sample_rate(budget_s, H=32, B=512):
+def oracle_sample_rate(budget_s, H=32):
     """The float64 oracle on a bounded sample of the headline workload: (GB/s, rows, seconds)."""
     from oracle import kda_oracle as ko
     case = synth.recurrent_case(8, H, 9, seed=0)
@@ -366,31 +421,32 @@ def oracle_sample_rate(budget_s, H=32, B=512):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    gbs = bytes_t1(rows, 0, H, 4) / el / 1e9
-    return gbs, rows, el
+    return bytes_t1(rows, 0, H, 4) / el / 1e9, rows, el
 
 
 def run_reference(args, rank, world):
+    """The float64 oracle as the reference arm, timed on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    H, B = HEADLINE["H"], HEADLINE["B"]
-    per_step = []
-    rows_total = 0
+    H, B = 32, 512
+    rates, rows_total = [], 0
     for i in range(args.warmup + args.steps):
-        gbs, rows, el = oracle_sample_rate(1.0, H, B)
+        gbs, rows, _ = oracle_sample_rate(1.0, H)
         if i >= args.warmup:
-            per_step.append((gbs, el))
+            rates.append(gbs)
             rows_total += rows
-    gbs = statistics.median(g for g, _ in per_step)
+    gbs = statistics.median(rates)
     us_call = bytes_t1(B, 0, H, 4) / (gbs * 1e9) * 1e6
+    cfg = dict(workload="kimi_linear_t1_recurrent", H=H, B=B, num_slots=1024, state="float32",
+               activations="bfloat16", gate="softplus",
+               sample="8 rows x 32 heads per oracle call, repeated for about 1 s per step")
     line = {
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_call / 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(HEADLINE, sample="8 rows x 32 heads per oracle call, repeated for ~1 s per step",
-                       note="float64 numpy oracle on the host cores, one thread"),
+        "config": cfg,
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{rows_total} rows x 32 heads over {args.steps} steps"},
+                         "sample": f"{rows_total} rows x 32 heads over {args.steps} steps, float64 numpy"},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -399,13 +455,19 @@ def run_reference(args, rank, world):
 # ---- main -------------------------------------------------------------------------------
 
 def main():
-    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap = argparse.ArgumentParser(description="KDA decode benchmark (GB300)")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=("recurrent", "packed", "fused", "spec"), default="recurrent")
+    ap.add_argument("--batch", type=int, default=0, help="rows (B / rows / N); 0 = the workload's default")
+    ap.add_argument("--heads", type=int, default=0)
+    ap.add_argument("--slots", type=int, default=0)
+    ap.add_argument("--t-max", type=int, default=0)
     ap.add_argument("--no-paths", action="store_true", help="skip the per-path / per-batch measurements")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU baseline budget")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end measurement")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU baseline budget (0 = skip)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -427,6 +489,12 @@ def main():
         if dist is not None:
             dist.barrier()
 
+    def max_over_ranks(x):
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        if dist is not None:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
     from linear_attention_decode_02_gb300 import build
     if rank == 0:
         build.build()
@@ -437,25 +505,28 @@ def main():
     peak = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
     peak_src = "measured" if peaks and peaks.get("hbm_gbs") else "fallback"
 
-    ms, nbytes, clocks, d, out = headline(args, rank, world, barrier, peaks)
-    t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    value = world * nbytes / (ms_max * 1e-3) / 1e9
-    achieved = nbytes / (ms * 1e-3) / 1e9
+    wl = make_workload(args, seed=rank)
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    ms, (w0, w1) = time_direct(wl.step, args.steps, args.warmup, barrier)
+    clocks.stop()
+    ms_max = max_over_ranks(ms)
+    value = world * wl.nbytes / (ms_max * 1e-3) / 1e9
+    achieved = wl.nbytes / (ms * 1e-3) / 1e9
 
-    e2e_ms, h2d, d2h = e2e_recurrent(d, max(20, args.steps // 4), 3, barrier)
-    t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    e2e_value = world * nbytes / (float(t.item()) * 1e-3) / 1e9
-    del d, out
+    e2e_obj = None
+    if not args.no_e2e:
+        e_ms, h2d, d2h = e2e(wl, max(20, args.steps // 4), 3, barrier)
+        e_max = max_over_ranks(e_ms)
+        e2e_obj = {"value": round(world * wl.nbytes / (e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_max, 5)}
+    name, cfg, nbytes = wl.name, dict(wl.config), wl.nbytes
+    del wl
     torch.cuda.empty_cache()
 
     paths = None
     if not args.no_paths and rank == 0:
-        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
         paths = path_measurements(flush, peak)
         del flush
 
@@ -466,23 +537,18 @@ def main():
                "sample": f"{rows} rows x 32 heads of the headline workload in {el:.1f} s, float64 numpy, one thread"}
 
     if rank == 0:
+        cfg.update(bytes_per_call=nbytes, parallelism=f"replicas x{world}",
+                   l2=("inputs larger than L2" if nbytes > L2_BYTES else "state smaller than L2: slot sets rotate")
+                   + "; slot sets alternate between steps")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms_max, 5), "us_per_call": round(ms_max * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic",
-            "config": dict(HEADLINE, bytes_per_call=nbytes,
-                           l2="inputs larger than L2: 1.07 GB of state per step, two disjoint slot sets alternate",
-                           parallelism=f"replicas x{world}"),
-            "gpu_launches": args.steps,
+            "data": "synthetic", "config": cfg, "gpu_launches": args.steps,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic("recurrent_h32_f32_b512"),
+                         "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name), "kernel": name,
                          "peak_source": f"{peak_src} copy bandwidth (burst)"},
-            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
-            "clocks": clocks,
-            "cpu_baseline": cpu,
-            "paths": paths,
+            "e2e": e2e_obj, "clocks": clocks.summary(w0, w1), "cpu_baseline": cpu, "paths": paths,
             "kernel_source_hash": kernel_source_hash(),
         }
         print(json.dumps(line))

@@ -238,7 +238,15 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
   KDA_CHECK(info->cc_major == 10 && info->cc_minor == 3, KDA_ERR_UNSUPPORTED,
             "device %d is compute capability %d.%d; this library is built for sm_103a (GB300) only", dev,
             info->cc_major, info->cc_minor);
+  // The stream's device is checked outside graph capture only: the query is
+  // not permitted on a capturing stream (a capture on a stream of another
+  // device fails at launch instead).
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (stream != nullptr) {
+    e = cudaStreamIsCapturing(stream, &cap);
+    KDA_CHECK(e == cudaSuccess, KDA_ERR_INVALID_ARG, "stream: %s", cudaGetErrorString(e));
+  }
+  if (stream != nullptr && cap == cudaStreamCaptureStatusNone) {
     int sdev = -1;
     e = cudaStreamGetDevice(stream, &sdev);
     KDA_CHECK(e == cudaSuccess, KDA_ERR_INVALID_ARG, "stream: %s", cudaGetErrorString(e));

@@ -73,7 +73,7 @@ def with_nulls(gen, slots, null_count, null_values=(-1,)):
 
 
 def recurrent_case(B, H, num_slots, seed=0, in_dtype=torch.bfloat16,
-                   state_dtype=torch.float32, state_indices=None, null_count=0):
+                   state_dtype=torch.float32, state_indices=None, null_count=0, make_state=True):
     """Inputs of the split q/k/v T=1 path (``kda_recurrent_decode``)."""
     gen = _gen(seed)
     case = {
@@ -90,7 +90,8 @@ def recurrent_case(B, H, num_slots, seed=0, in_dtype=torch.bfloat16,
     else:
         idx = torch.tensor(state_indices, dtype=torch.int32)
     case["state_indices"] = idx
-    case["state"] = state_pool(gen, num_slots, H, state_dtype)
+    if make_state:
+        case["state"] = state_pool(gen, num_slots, H, state_dtype)
     return case
 
 
@@ -100,7 +101,7 @@ def tiny_recurrent_case(seed=0):
                           state_dtype=torch.float32, state_indices=[3, 1, -1, 6])
 
 
-def packed_case(B, num_slots=2048, seed=0, null_frac=0.1, heads=12):
+def packed_case(B, num_slots=2048, seed=0, null_frac=0.1, heads=12, make_state=True):
     """Inputs of the Kimi K3 packed T=1 path (``kda_packed_decode``)."""
     gen = _gen(seed)
     HD = heads * D
@@ -113,7 +114,8 @@ def packed_case(B, num_slots=2048, seed=0, null_frac=0.1, heads=12):
     }
     n_null = int(math.floor(null_frac * B))
     case["state_indices"] = with_nulls(gen, distinct_slots(gen, B, num_slots), n_null)
-    case["state"] = state_pool(gen, num_slots, heads, torch.bfloat16)
+    if make_state:
+        case["state"] = state_pool(gen, num_slots, heads, torch.bfloat16)
     return case
 
 
@@ -127,7 +129,7 @@ def conv_cache(gen, num_slots, channels):
 
 
 def fused_case(H, rows, seed=0, state_dtype=torch.float32, null_frac=0.1,
-               num_slots=None, gate_4d=True):
+               num_slots=None, gate_4d=True, make_state=True):
     """Inputs of the fused conv + KDA + gated RMSNorm path (``kda_fused_decode``)."""
     gen = _gen(seed)
     HD = H * D
@@ -144,8 +146,9 @@ def fused_case(H, rows, seed=0, state_dtype=torch.float32, null_frac=0.1,
     n_null = int(math.floor(null_frac * rows))
     case["state_indices"] = with_nulls(gen, distinct_slots(gen, rows, num_slots), n_null,
                                        null_values=(0, -1))
-    case["conv_state"] = conv_cache(gen, num_slots, 3 * HD)
-    case["state"] = state_pool(gen, num_slots, H, state_dtype)
+    if make_state:
+        case["conv_state"] = conv_cache(gen, num_slots, 3 * HD)
+        case["state"] = state_pool(gen, num_slots, H, state_dtype)
     og = _normal(gen, (rows, H, D), dtype=torch.bfloat16)
     case["output_gate"] = og.unsqueeze(0) if gate_4d else og
     case["norm_weight"] = _normal(gen, (D,), std=0.1, mean=1.0)
@@ -166,7 +169,7 @@ def spec_lengths(gen, N, t_max, empty_frac=0.125):
 
 
 def spec_case(N, t_max, seed=0, H=16, lengths=None, pad_rows=0, null_count=0,
-              state_dtype=torch.float32, num_slots=None):
+              state_dtype=torch.float32, num_slots=None, make_state=True):
     """Inputs of the packed speculative path (``kda_spec_decode``).
 
     Token rows [cu[N], cu[N] + pad_rows) are graph padding past the last row.
@@ -192,7 +195,8 @@ def spec_case(N, t_max, seed=0, H=16, lengths=None, pad_rows=0, null_count=0,
         "t_max": int(t_max),
     }
     case["state_indices"] = with_nulls(gen, distinct_slots(gen, N, num_slots), null_count)
-    case["state"] = state_pool(gen, num_slots, H, state_dtype)
+    if make_state:
+        case["state"] = state_pool(gen, num_slots, H, state_dtype)
     return case
 
 
