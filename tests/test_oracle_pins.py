@@ -69,8 +69,8 @@ def test_softplus_gate_identities():
     A_log = np.array([-2.0, -0.5, 0.0])
     g = ko.gate_softplus(raw, dt, A_log)
     assert np.all(g < 0)
-    # at raw + dt = 0 the gate is -exp(A_log) * ln 2
-    g0 = ko.gate_softplus(np.zeros((H, 128)), np.zeros((H, 128)), A_log)
+    # at raw + dt = 0 the gate is -exp(A_log) * ln 2 (dt_bias shifts the raw gate)
+    g0 = ko.gate_softplus(-dt, dt, A_log)
     np.testing.assert_allclose(g0, -np.exp(A_log)[:, None] * np.log(2.0) * np.ones((H, 128)),
                                rtol=1e-15)
     # A_log -> -inf switches the decay off
@@ -91,6 +91,8 @@ def test_lower_bound_gate_identities():
     assert np.all(g < 0) and np.all(g > lb)
     g0 = ko.gate_lower_bound(np.zeros((H, 128)), dt, A_log, lb)
     np.testing.assert_array_equal(g0, np.full((H, 128), lb / 2))
+    shift = 0.3 * rng.standard_normal((H, 128))
+    np.testing.assert_allclose(ko.gate_lower_bound(-shift, shift, A_log, lb), lb / 2, rtol=1e-15)
     # large positive argument saturates at the bound, large negative at zero
     np.testing.assert_allclose(ko.gate_lower_bound(np.full((H, 128), 80.0), dt, A_log, lb),
                                lb, rtol=1e-12)
