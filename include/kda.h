@@ -200,9 +200,38 @@ int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t
  * Force the split of every later call in this process (0 restores the
  * measured policy).  For sweeps and tests.  Returns KDA_ERR_INVALID_ARG for
  * a split this build has no kernel for (the fused entry point always uses
- * split 1 and ignores the override).
+ * split 1 and ignores the override).  A forced split selects the split
+ * schedule for the T=1 entry points unless a schedule is forced too.
  */
 kda_status kda_set_split_override(int32_t split);
+
+/*
+ * Kernel schedules of the T=1 entry points (kda_recurrent_decode,
+ * kda_packed_decode).  SPLIT: one CTA per (row, head, value split), the
+ * state block streamed through registers; best for latency-bound batches.
+ * STREAM: one persistent CTA per SM, a producer warp moving whole state
+ * blocks into shared-memory stages with bulk asynchronous copies while
+ * consumer warps update the previous ones; needs every q / k / v / gate
+ * head vector 16-byte aligned (otherwise the call uses SPLIT, or returns
+ * KDA_ERR_UNSUPPORTED if STREAM is forced).
+ */
+typedef enum kda_schedule { KDA_SCHED_AUTO = 0, KDA_SCHED_SPLIT = 1, KDA_SCHED_STREAM = 2 } kda_schedule;
+
+/* Schedule the dispatcher picks (same arguments as kda_plan_split); 0 on invalid arguments. */
+int32_t kda_plan_schedule(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max,
+                          int32_t sm_count);
+
+/* Force the schedule of later T=1 calls (KDA_SCHED_AUTO restores the policy). */
+kda_status kda_set_schedule_override(int32_t schedule);
+
+/*
+ * Device error word of the streaming kernels on the current device: bit 0 =
+ * a wait for a filled stage timed out (2 s), bit 1 = a wait for a free stage
+ * timed out.  A kernel that times out records the bit and returns early, its
+ * results for the affected units are undefined.  Synchronises the device;
+ * clears the word when `clear` is non-zero.
+ */
+kda_status kda_device_error(uint32_t* flags, int32_t clear);
 
 const char* kda_status_string(kda_status s);
 /* Detail of the last non-OK status returned on the calling thread. */

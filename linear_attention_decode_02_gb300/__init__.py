@@ -10,6 +10,7 @@ The four decode entry points of libkda, with the C names:
 Build the library with ``python -m linear_attention_decode_02_gb300.build``.
 """
 
-from .binding import (KdaError, kda_fused_decode, kda_packed_decode, kda_plan_split,  # noqa: F401
-                      kda_recurrent_decode, kda_set_split_override, kda_spec_decode, kda_version,
-                      library)
+from .binding import (SCHED_AUTO, SCHED_SPLIT, SCHED_STREAM, KdaError, kda_device_error,  # noqa: F401
+                      kda_fused_decode, kda_packed_decode, kda_plan_schedule, kda_plan_split,
+                      kda_recurrent_decode, kda_set_schedule_override, kda_set_split_override,
+                      kda_spec_decode, kda_version, library)

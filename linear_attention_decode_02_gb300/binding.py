@@ -30,8 +30,9 @@ DEFAULT_SCALE = 1.0 / math.sqrt(128.0)
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_recurrent_decode", "kda_packed_decode", "kda_fused_decode", "kda_spec_decode",
-           "kda_plan_split", "kda_set_split_override", "kda_status_string",
-           "kda_last_error_message", "kda_version")
+           "kda_plan_split", "kda_set_split_override", "kda_plan_schedule", "kda_set_schedule_override",
+           "kda_device_error", "kda_status_string", "kda_last_error_message", "kda_version")
+SCHED_AUTO, SCHED_SPLIT, SCHED_STREAM = 0, 1, 2
 
 
 class KdaError(RuntimeError):
@@ -64,6 +65,12 @@ def _declare(lib):
     lib.kda_plan_split.restype = i32
     lib.kda_set_split_override.argtypes = [i32]
     lib.kda_set_split_override.restype = ctypes.c_int
+    lib.kda_plan_schedule.argtypes = [i32, ctypes.c_int64, i32, i32, i32]
+    lib.kda_plan_schedule.restype = i32
+    lib.kda_set_schedule_override.argtypes = [i32]
+    lib.kda_set_schedule_override.restype = ctypes.c_int
+    lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
+    lib.kda_device_error.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_last_error_message.argtypes = []
@@ -185,6 +192,25 @@ def kda_set_split_override(split):
     """Force every later call's split (0 restores the policy)."""
     lib = library()
     _check(lib, lib.kda_set_split_override(int(split)))
+
+
+def kda_plan_schedule(op, units, state_dtype, t_max, sm_count):
+    """Schedule the dispatcher picks (host-only query)."""
+    return int(library().kda_plan_schedule(int(op), int(units), int(state_dtype), int(t_max), int(sm_count)))
+
+
+def kda_set_schedule_override(schedule):
+    """Force the T=1 schedule (SCHED_SPLIT / SCHED_STREAM; SCHED_AUTO restores the policy)."""
+    lib = library()
+    _check(lib, lib.kda_set_schedule_override(int(schedule)))
+
+
+def kda_device_error(clear=True):
+    """Device error word of the streaming kernels (synchronises the device)."""
+    lib = library()
+    flags = ctypes.c_uint32(0)
+    _check(lib, lib.kda_device_error(ctypes.byref(flags), int(bool(clear))))
+    return int(flags.value)
 
 
 def kda_version():

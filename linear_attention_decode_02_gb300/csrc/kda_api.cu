@@ -23,6 +23,7 @@ constexpr int64_t kUnit = kD * kD;  // elements of one (slot, head) state block
 
 thread_local std::string g_last_error;
 std::atomic<int> g_split_override{0};
+std::atomic<int> g_schedule_override{KDA_SCHED_AUTO};
 
 kda_status fail(kda_status st, const char* fmt, ...) {
   char buf[512];
@@ -255,6 +256,26 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
   return KDA_OK;
 }
 
+// T=1 schedule: the persistent streaming kernel once the units fill several
+// waves of the SMs, the split kernel below that (latency-bound sizes).
+int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
+  (void)state_dtype;
+  (void)t_max;
+  if (op != KDA_OP_RECURRENT && op != KDA_OP_PACKED) return KDA_SCHED_SPLIT;
+  const int forced = g_schedule_override.load();
+  if (forced != KDA_SCHED_AUTO) return forced;
+  if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
+  return units >= 4LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
+}
+
+// Every head vector of the view starts on a 16-byte boundary (bulk copies).
+bool rows_aligned16(const View& v) {
+  if (reinterpret_cast<uintptr_t>(v.data) % 16 != 0) return false;
+  for (int i = 0; i < v.ndim - 1; ++i)
+    if (v.shape[i] > 1 && (v.stride[i] * esize(v.dtype)) % 16 != 0) return false;
+  return true;
+}
+
 int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)state_dtype;
   (void)t_max;
@@ -340,7 +361,15 @@ kda_status kda_recurrent_decode(const kda_tensor* q, const kda_tensor* k, const 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DeviceInfo dev;
   KDA_TRY(current_device(st, &dev));
-  const int split = plan_split(KDA_OP_RECURRENT, B * H, S.dtype, 1, dev.sms);
+  int sched = plan_schedule(KDA_OP_RECURRENT, B * H, S.dtype, 1, dev.sms);
+  const bool stream_ok = rows_aligned16(Q) && rows_aligned16(K) && rows_aligned16(V) && rows_aligned16(G) &&
+                         B * H <= INT32_MAX;
+  if (sched == KDA_SCHED_STREAM && !stream_ok) {
+    KDA_CHECK(g_schedule_override.load() != KDA_SCHED_STREAM, KDA_ERR_UNSUPPORTED,
+              "stream schedule forced but an activation head vector is not 16-byte aligned");
+    sched = KDA_SCHED_SPLIT;
+  }
+  const int split = sched == KDA_SCHED_STREAM ? 1 : plan_split(KDA_OP_RECURRENT, B * H, S.dtype, 1, dev.sms);
   KDA_CHECK(kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
   KDA_TRY(check_grid(B * H * split));
 
@@ -359,6 +388,7 @@ kda_status kda_recurrent_decode(const kda_tensor* q, const kda_tensor* k, const 
   a.out = O.data; a.B = (int32_t)B; a.H = (int32_t)H;
   a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
   a.lower_bound = lower_bound; a.scale = scale;
+  if (sched == KDA_SCHED_STREAM) return check_launch(kda::launch_t1_stream(a, S.dtype, dev.sms, st));
   return check_launch(kda::launch_t1(a, S.dtype, split, st));
 }
 
@@ -402,7 +432,13 @@ kda_status kda_packed_decode(const kda_tensor* mixed_qkv, const kda_tensor* raw_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DeviceInfo dev;
   KDA_TRY(current_device(st, &dev));
-  const int split = plan_split(KDA_OP_PACKED, B * H, S.dtype, 1, dev.sms);
+  int sched = plan_schedule(KDA_OP_PACKED, B * H, S.dtype, 1, dev.sms);
+  if (sched == KDA_SCHED_STREAM && !(rows_aligned16(M) && rows_aligned16(G))) {
+    KDA_CHECK(g_schedule_override.load() != KDA_SCHED_STREAM, KDA_ERR_UNSUPPORTED,
+              "stream schedule forced but a packed row is not 16-byte aligned");
+    sched = KDA_SCHED_SPLIT;
+  }
+  const int split = sched == KDA_SCHED_STREAM ? 1 : plan_split(KDA_OP_PACKED, B * H, S.dtype, 1, dev.sms);
   KDA_CHECK(kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
   KDA_TRY(check_grid(B * H * split));
 
@@ -422,6 +458,7 @@ kda_status kda_packed_decode(const kda_tensor* mixed_qkv, const kda_tensor* raw_
   a.gate_mode = kda::KDA_GATE_LOWER_BOUND;
   a.lower_bound = -5.0f;
   a.scale = 0.08838834764831845f;  // 1/sqrt(128)
+  if (sched == KDA_SCHED_STREAM) return check_launch(kda::launch_t1_stream(a, S.dtype, dev.sms, st));
   return check_launch(kda::launch_t1(a, S.dtype, split, st));
 }
 
@@ -593,6 +630,28 @@ int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t
   if (op < KDA_OP_RECURRENT || op > KDA_OP_SPEC || units < 0 || sm_count < 1 || t_max < 1) return 0;
   if (state_dtype != KDA_F32 && state_dtype != KDA_BF16) return 0;
   return plan_split(op, units, state_dtype, t_max, sm_count);
+}
+
+int32_t kda_plan_schedule(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max, int32_t sm_count) {
+  if (op < KDA_OP_RECURRENT || op > KDA_OP_SPEC || units < 0 || sm_count < 1 || t_max < 1) return 0;
+  if (state_dtype != KDA_F32 && state_dtype != KDA_BF16) return 0;
+  return plan_schedule(op, units, state_dtype, t_max, sm_count);
+}
+
+kda_status kda_set_schedule_override(int32_t schedule) {
+  KDA_CHECK(schedule == KDA_SCHED_AUTO || schedule == KDA_SCHED_SPLIT || schedule == KDA_SCHED_STREAM,
+            KDA_ERR_INVALID_ARG, "unknown schedule %d", schedule);
+  g_schedule_override.store(schedule);
+  return KDA_OK;
+}
+
+kda_status kda_device_error(uint32_t* flags, int32_t clear) {
+  KDA_CHECK(flags != nullptr, KDA_ERR_INVALID_ARG, "flags: null pointer");
+  unsigned int f = 0;
+  cudaError_t e = kda::read_device_error(&f, clear != 0);
+  KDA_CHECK(e == cudaSuccess, KDA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+  *flags = f;
+  return KDA_OK;
 }
 
 kda_status kda_set_split_override(int32_t split) {

@@ -68,6 +68,14 @@ cudaError_t launch_t1(const T1Args& a, int state_dtype, int split, cudaStream_t 
 cudaError_t launch_fused(const FusedArgs& a, int state_dtype, cudaStream_t s);
 cudaError_t launch_spec(const SpecArgs& a, int state_dtype, int split, cudaStream_t s);
 
+// Persistent streaming T=1 kernel (bulk copies into shared-memory stages);
+// needs 16-byte aligned q / k / v / gate head vectors.
+cudaError_t launch_t1_stream(const T1Args& a, int state_dtype, int sm_count, cudaStream_t s);
+
+// Reads (and optionally clears) the device error word of the streaming
+// kernels: bit 0 = a stage-full wait timed out, bit 1 = a stage-free wait.
+cudaError_t read_device_error(unsigned int* flags, bool clear);
+
 // Splits with a compiled kernel (1, 2, 4, 8, 16).
 bool split_supported(int split);
 

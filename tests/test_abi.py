@@ -248,3 +248,21 @@ def test_spec_contract(lib):
     t = _spec_args(R=0)
     t["cu_seqlens"] = torch.zeros(4, dtype=torch.int32)
     assert _call_spec(lib, t) == OK  # no token rows: nothing to launch
+
+
+def test_schedule_override_and_plan(lib):
+    assert lib.kda_set_schedule_override(7) == INVALID
+    assert lib.kda_set_schedule_override(2) == OK
+    assert binding.kda_plan_schedule(0, 1, 0, 1, 152) == 2
+    assert binding.kda_plan_schedule(3, 1, 0, 1, 152) == 1  # spec has one schedule
+    assert lib.kda_set_schedule_override(0) == OK
+    assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 2
+    assert binding.kda_plan_schedule(1, 12, 1, 1, 152) == 1
+    assert lib.kda_set_split_override(8) == OK  # a forced split implies the split schedule
+    assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 1
+    assert lib.kda_set_split_override(0) == OK
+    assert binding.kda_plan_schedule(9, 6144, 1, 1, 152) == 0
+
+
+def test_device_error_query_needs_a_pointer(lib):
+    assert lib.kda_device_error(None, 0) == INVALID

@@ -21,6 +21,7 @@ def lib():
     build.build()
     yield binding.library()
     binding.kda_set_split_override(0)
+    binding.kda_set_schedule_override(binding.SCHED_AUTO)
 
 
 def _run_recurrent(d, lower_bound=None, out=None):
@@ -238,3 +239,100 @@ def test_packed_long_run_drift_stays_bounded():
             ref_state[s] = st[s]
         worst = max(worst, float(np.abs(out.double().cpu().numpy().reshape(B, 12, 128) - ref_out).max()))
     assert worst <= P.OUT_ATOL
+
+
+# ---- persistent streaming schedule (bulk copies into shared-memory stages) -----------
+
+@pytest.fixture
+def stream_schedule():
+    binding.kda_set_schedule_override(binding.SCHED_STREAM)
+    yield
+    binding.kda_set_schedule_override(binding.SCHED_AUTO)
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("lower_bound", [None, -5.0])
+@pytest.mark.parametrize("B,H,N,nulls", [(3, 2, 8, 1), (37, 5, 60, 4)])
+def test_stream_schedule_parity(stream_schedule, state_dtype, in_dtype, lower_bound, B, H, N, nulls):
+    case = synth.recurrent_case(B, H, N, seed=B + H, in_dtype=in_dtype, state_dtype=state_dtype, null_count=nulls)
+    d = P.to_device(case)
+    before = d["state"].clone()
+    out = _run_recurrent(d, lower_bound=lower_bound)
+    torch.cuda.synchronize()
+    _check_recurrent(case, d, before, out, lower_bound=lower_bound)
+    assert binding.kda_device_error() == 0
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_stream_many_units_per_cta(stream_schedule, state_dtype):
+    """Thousands of units: every stage is refilled many times."""
+    case = synth.recurrent_case(300, 12, 400, seed=21, state_dtype=state_dtype, null_count=30)
+    d = P.to_device(case)
+    before = d["state"].clone()
+    out = _run_recurrent(d)
+    torch.cuda.synchronize()
+    rows = sorted(np.random.default_rng(2).choice(300, 60, replace=False).tolist())
+    _check_recurrent(case, d, before, out, rows=rows)
+    assert binding.kda_device_error() == 0
+
+
+def test_stream_needs_aligned_head_vectors(stream_schedule):
+    """Forced streaming on 8-byte-aligned rows is refused; the policy uses the split kernel instead."""
+    B, H = 40, 16
+    case = synth.recurrent_case(B, H, 64, seed=22)
+    d = P.to_device(case)
+    wide = torch.zeros(B, H * 128 + 4, dtype=torch.bfloat16, device="cuda")
+    wide[:, : H * 128] = d["q"].reshape(B, -1)
+    d["q"] = wide[:, : H * 128].view(B, H, 128)
+    assert (d["q"].stride(0) * 2) % 16 == 8
+    with pytest.raises(binding.KdaError) as e:
+        _run_recurrent(d)
+    assert e.value.status == 2
+    binding.kda_set_schedule_override(binding.SCHED_AUTO)
+    before = d["state"].clone()
+    out = _run_recurrent(d)
+    torch.cuda.synchronize()
+    _check_recurrent(case, d, before, out)
+
+
+def test_stream_graph_replay(stream_schedule):
+    B, H, N = 64, 32, 200
+    c1 = synth.recurrent_case(B, H, N, seed=23, null_count=5)
+    d = P.to_device(c1)
+    out = torch.empty(B, H, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run_recurrent(d, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    fresh = P.dev(c1["state"])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _run_recurrent(d, out=out)
+    c2 = synth.recurrent_case(B, H, N, seed=24, null_count=9)
+    for key in ("q", "k", "v", "raw_gate", "raw_beta", "state_indices"):
+        d[key].copy_(c2[key].cuda())
+    c2["state"], c2["A_log"], c2["dt_bias"] = c1["state"], c1["A_log"], c1["dt_bias"]
+    d["state"].copy_(fresh)
+    before = d["state"].clone()
+    g.replay()
+    torch.cuda.synchronize()
+    _check_recurrent(c2, d, before, out)
+
+
+@pytest.mark.parametrize("B", [5, 100])
+def test_packed_stream_schedule(stream_schedule, B):
+    case = synth.packed_case(B, num_slots=256, seed=25 + B)
+    d = P.to_device(case)
+    before = d["state"].clone()
+    out = _run_packed(d)
+    torch.cuda.synchronize()
+    _check_packed(case, d, before, out)
+    assert binding.kda_device_error() == 0
+
+
+def test_schedule_policy_queries():
+    assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == binding.SCHED_STREAM
+    assert binding.kda_plan_schedule(0, 32, 0, 1, 152) == binding.SCHED_SPLIT
+    assert binding.kda_plan_schedule(2, 16384, 0, 1, 152) == binding.SCHED_SPLIT
