@@ -336,3 +336,24 @@ def test_schedule_policy_queries():
     assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == binding.SCHED_STREAM
     assert binding.kda_plan_schedule(0, 32, 0, 1, 152) == binding.SCHED_SPLIT
     assert binding.kda_plan_schedule(2, 16384, 0, 1, 152) == binding.SCHED_SPLIT
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_stream_guard_bands_between_slots(stream_schedule, state_dtype):
+    """Stream schedule on a pool whose slot stride exceeds the slot block (tensor-map strides)."""
+    B, H, N = 40, 6, 50
+    case = synth.recurrent_case(B, H, N, seed=26, state_dtype=state_dtype, null_count=3)
+    block = H * 128 * 128
+    stride = block + 8192
+    buf = torch.full((N * stride,), 7.25, dtype=state_dtype, device="cuda")
+    pool = torch.as_strided(buf, (N, H, 128, 128), (stride, 128 * 128, 128, 1))
+    pool.copy_(case["state"].cuda())
+    d = P.to_device(case)
+    d["state"] = pool
+    gaps = buf.view(N, stride)[:, block:].clone()
+    before = pool.clone()
+    out = _run_recurrent(d)
+    torch.cuda.synchronize()
+    assert torch.equal(buf.view(N, stride)[:, block:], gaps)
+    _check_recurrent(case, d, before, out)
+    assert binding.kda_device_error() == 0
