@@ -234,10 +234,11 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the device-code sources (the host dispatcher kda_api.cu excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_attention_decode_02_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name != "kda_api.cu":
             with open(os.path.join(csrc, name), "rb") as f:
                 h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]

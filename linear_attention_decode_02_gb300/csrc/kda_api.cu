@@ -265,7 +265,9 @@ int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   const int forced = g_schedule_override.load();
   if (forced != KDA_SCHED_AUTO) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
-  return units >= 4LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
+  // Measured on GB300 (152 SMs): the streaming kernel wins from about five
+  // units per SM (Kimi-Linear H=32 B>=24, packed K3 B>=64).
+  return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
 }
 
 // Every head vector of the view starts on a 16-byte boundary (bulk copies).
@@ -282,10 +284,10 @@ int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   const int forced = g_split_override.load();
   if (op == KDA_OP_FUSED) return 1;
   if (forced != 0) return forced;
-  // Smallest split whose CTA count reaches two waves of the SMs.
-  int split = 1;
-  while (split < 16 && units * split < 2LL * sms) split *= 2;
-  return split;
+  // Measured on GB300 for the split kernel (used below the streaming
+  // threshold): 16 value slabs per unit while the units are fewer than half
+  // the SMs, 8 above.  Longer speculative rows keep 8 as well.
+  return 2 * units <= sms ? 16 : 8;
 }
 
 kda_status check_launch(cudaError_t e) {

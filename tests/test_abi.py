@@ -43,9 +43,11 @@ def test_status_strings_and_version(lib):
 
 
 def test_plan_split_policy(lib):
-    # two waves of CTAs on 152 SMs: split doubles until units * split >= 304
-    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 1
+    # split kernel: 16 slabs per unit below half the SM count, 8 above
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 8
     assert binding.kda_plan_split(0, 32, 0, 1, 152) == 16
+    assert binding.kda_plan_split(0, 76, 0, 1, 152) == 16
+    assert binding.kda_plan_split(0, 77, 0, 1, 152) == 8
     assert binding.kda_plan_split(2, 8, 0, 1, 152) == 1  # fused is always split 1
     assert binding.kda_plan_split(0, 1, 5, 1, 152) == 0  # bad dtype
     assert binding.kda_plan_split(9, 1, 0, 1, 152) == 0  # bad op
@@ -60,7 +62,7 @@ def test_split_override(lib):
     assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
     assert binding.kda_plan_split(2, 16384, 0, 1, 152) == 1
     assert lib.kda_set_split_override(0) == OK
-    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 1
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 8
 
 
 def _recurrent_args(B=2, H=2, N=4, qkv=torch.bfloat16, state=torch.float32):
