@@ -322,6 +322,21 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
+# ---- rank aggregation ------------------------------------------------------------------
+
+def reduce_max(x, dist=None, device="cpu"):
+    """Max of a per-rank float over the process group (identity without one)."""
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_gbs(bytes_per_rank, world, ms_max):
+    """Whole-job GB/s: every rank's bytes over the slowest rank's time per step."""
+    return world * bytes_per_rank / (ms_max * 1e-3) / 1e9
+
+
 # ---- timing helpers ------------------------------------------------------------------
 
 def time_direct(fn, steps, warmup, barrier):
@@ -491,10 +506,7 @@ def main():
             dist.barrier()
 
     def max_over_ranks(x):
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
-        if dist is not None:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, dist, "cuda")
 
     from linear_attention_decode_02_gb300 import build
     if rank == 0:
@@ -512,14 +524,14 @@ def main():
     ms, (w0, w1) = time_direct(wl.step, args.steps, args.warmup, barrier)
     clocks.stop()
     ms_max = max_over_ranks(ms)
-    value = world * wl.nbytes / (ms_max * 1e-3) / 1e9
+    value = job_gbs(wl.nbytes, world, ms_max)
     achieved = wl.nbytes / (ms * 1e-3) / 1e9
 
     e2e_obj = None
     if not args.no_e2e:
         e_ms, h2d, d2h = e2e(wl, max(20, args.steps // 4), 3, barrier)
         e_max = max_over_ranks(e_ms)
-        e2e_obj = {"value": round(world * wl.nbytes / (e_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+        e2e_obj = {"value": round(job_gbs(wl.nbytes, world, e_max), 1), "unit": "GB/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_max, 5)}
     name, cfg, nbytes = wl.name, dict(wl.config), wl.nbytes
     del wl

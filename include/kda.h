@@ -207,13 +207,16 @@ kda_status kda_set_split_override(int32_t split);
 
 /*
  * Kernel schedules of the T=1 entry points (kda_recurrent_decode,
- * kda_packed_decode).  SPLIT: one CTA per (row, head, value split), the
- * state block streamed through registers; best for latency-bound batches.
- * STREAM: one persistent CTA per SM, a producer warp moving whole state
- * blocks into shared-memory stages with bulk asynchronous copies while
- * consumer warps update the previous ones; needs every q / k / v / gate
- * head vector 16-byte aligned (otherwise the call uses SPLIT, or returns
- * KDA_ERR_UNSUPPORTED if STREAM is forced).
+ * kda_packed_decode, kda_fused_decode).  SPLIT: one CTA per (row, head,
+ * value split; the fused entry point always uses one split), the state
+ * block streamed through registers; best for latency-bound batches.
+ * STREAM: one persistent CTA per SM, a loader warp moving whole state
+ * blocks (TMA, swizzled) and the unit's activation vectors into
+ * shared-memory stages with bulk asynchronous copies while consumer warps
+ * update earlier ones; needs every activation head vector (and, fused, the
+ * conv-cache slots) 16-byte aligned, otherwise the call uses SPLIT, or
+ * returns KDA_ERR_UNSUPPORTED if STREAM is forced.  kda_spec_decode has the
+ * split schedule only.
  */
 typedef enum kda_schedule { KDA_SCHED_AUTO = 0, KDA_SCHED_SPLIT = 1, KDA_SCHED_STREAM = 2 } kda_schedule;
 

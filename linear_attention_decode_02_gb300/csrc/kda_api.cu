@@ -261,7 +261,7 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
 int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)state_dtype;
   (void)t_max;
-  if (op != KDA_OP_RECURRENT && op != KDA_OP_PACKED) return KDA_SCHED_SPLIT;
+  if (op == KDA_OP_SPEC) return KDA_SCHED_SPLIT;
   const int forced = g_schedule_override.load();
   if (forced != KDA_SCHED_AUTO) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
@@ -535,6 +535,15 @@ kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, 
   DeviceInfo dev;
   KDA_TRY(current_device(st, &dev));
   KDA_TRY(check_grid(rows * H));
+  int sched = plan_schedule(KDA_OP_FUSED, rows * H, S.dtype, 1, dev.sms);
+  const bool stream_ok = rows_aligned16(X) && rows_aligned16(G) && rows_aligned16(OG) &&
+                         reinterpret_cast<uintptr_t>(C.data) % 16 == 0 &&
+                         (C.shape[0] <= 1 || (C.stride[0] * 2) % 16 == 0) && rows * H <= INT32_MAX;
+  if (sched == KDA_SCHED_STREAM && !stream_ok) {
+    KDA_CHECK(g_schedule_override.load() != KDA_SCHED_STREAM, KDA_ERR_UNSUPPORTED,
+              "stream schedule forced but an activation row or conv-cache slot is not 16-byte aligned");
+    sched = KDA_SCHED_SPLIT;
+  }
 
   kda::FusedArgs a{};
   a.x = X.data; a.x_rs = X.stride[0];
@@ -552,6 +561,7 @@ kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, 
   a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
   a.lower_bound = lower_bound; a.norm_eps = norm_eps;
   a.scale = 0.08838834764831845f;  // 1/sqrt(128)
+  if (sched == KDA_SCHED_STREAM) return check_launch(kda::launch_fused_stream(a, S.dtype, dev.sms, st));
   return check_launch(kda::launch_fused(a, S.dtype, st));
 }
 

@@ -72,6 +72,10 @@ cudaError_t launch_spec(const SpecArgs& a, int state_dtype, int split, cudaStrea
 // needs 16-byte aligned q / k / v / gate head vectors.
 cudaError_t launch_t1_stream(const T1Args& a, int state_dtype, int sm_count, cudaStream_t s);
 
+// Persistent streaming fused kernel; needs 16-byte aligned x rows, conv-cache
+// slots, raw-gate and output-gate head vectors.
+cudaError_t launch_fused_stream(const FusedArgs& a, int state_dtype, int sm_count, cudaStream_t s);
+
 // Reads (and optionally clears) the device error word of the streaming
 // kernels: bit 0 = a stage-full wait timed out, bit 1 = a stage-free wait.
 cudaError_t read_device_error(unsigned int* flags, bool clear);

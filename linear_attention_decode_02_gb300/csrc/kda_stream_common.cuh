@@ -1,0 +1,136 @@
+// Shared pieces of the persistent streaming kernels: stage geometry, the
+// 128-byte swizzle of TMA-loaded state blocks, shared-memory activation
+// reads, the 3-d tensor-map load, named-barrier votes, and the tensor-map
+// encoder entry point.
+#pragma once
+
+#include <cuda.h>
+
+#include "kda_async.cuh"
+#include "kda_kernels.cuh"
+
+namespace kda {
+
+// A state block (128 x 128) arrives as NBLK column blocks of 128 rows x 128
+// bytes, each 128-byte swizzled (16-byte chunk index XOR row % 8).
+template <typename StateT>
+struct SwzCfg {
+  static constexpr int BLK_COLS = 128 / sizeof(StateT);  // 32 (f32) or 64 (bf16) columns
+  static constexpr int NBLK = kD / BLK_COLS;             // 4 (f32) or 2 (bf16) blocks per state
+  static constexpr uint32_t BLK_BYTES = kD * 128;        // 128 rows x 128 bytes
+  static constexpr uint32_t STATE_BYTES = NBLK * BLK_BYTES;
+};
+
+// Ring of NSTAGE stages: [state block | ACT_BYTES of unit vectors] each
+// (1024-byte aligned), then per stage a coefficient array (128 float4),
+// DERIVED_BYTES of prologue results, scalars (int4) and three mbarriers.
+template <typename StateT, uint32_t ACT_BYTES, int NSTAGE_, uint32_t DERIVED_BYTES = 0>
+struct StageCfg : SwzCfg<StateT> {
+  static constexpr int NSTAGE = NSTAGE_;
+  static constexpr int NW = 8;   // consumer warps
+  static constexpr int CW = 16;  // columns per consumer warp
+  static constexpr uint32_t STAGE_BYTES = ((SwzCfg<StateT>::STATE_BYTES + ACT_BYTES + 1023) / 1024) * 1024;
+  static constexpr size_t COEF_OFF = (size_t)NSTAGE * STAGE_BYTES;
+  static constexpr size_t DERIVED_OFF = COEF_OFF + (size_t)NSTAGE * kD * sizeof(float4);
+  static constexpr size_t SCAL_OFF = DERIVED_OFF + (size_t)NSTAGE * DERIVED_BYTES;
+  static constexpr size_t BAR_OFF = SCAL_OFF + (size_t)NSTAGE * sizeof(int4);
+  static constexpr size_t TAIL_OFF = BAR_OFF + 3 * NSTAGE * sizeof(uint64_t);  // kernel-specific extras
+  static_assert(CW * NW == kD, "consumers cover the 128 value columns");
+};
+
+// Lane -> first key row of its fragments, chosen so that the rows read by
+// one quarter-warp differ in bit 2 (f32: 2 rows) or bits 1-2 (bf16: 4 rows):
+// under the 128-byte swizzle those rows' chunks land in distinct banks.
+template <typename StateT>
+__device__ __forceinline__ int stream_row0(int lane);
+template <>
+__device__ __forceinline__ int stream_row0<float>(int lane) {  // 4 lanes per row, 8 rows per instruction
+  return (lane >> 3) + ((lane >> 2) & 1) * 4;
+}
+template <>
+__device__ __forceinline__ int stream_row0<__nv_bfloat16>(int lane) {  // 2 lanes per row, 16 rows
+  return ((lane >> 1) & 3) * 2 + ((lane >> 3) & 1) + ((lane >> 4) & 1) * 8;
+}
+
+// Byte offset of the 16-byte chunk holding (row, col) in a swizzled state block.
+template <typename StateT>
+__device__ __forceinline__ uint32_t swz_offset(int row, int col) {
+  using C = SwzCfg<StateT>;
+  const int blk = col / C::BLK_COLS;
+  const int chunk = (col % C::BLK_COLS) * (int)sizeof(StateT) / 16;
+  return blk * C::BLK_BYTES + row * 128 + ((chunk ^ (row & 7)) << 4);
+}
+
+// Four consecutive elements (float32 or bfloat16) of a shared-memory vector.
+__device__ __forceinline__ float4 lds4(const unsigned char* base, int i, int dtype) {
+  if (dtype == KDA_DT_F32) return reinterpret_cast<const float4*>(base)[i >> 2];
+  const uint2 u = reinterpret_cast<const uint2*>(base)[i >> 2];
+  return make_float4(bf_lo(u.x), bf_hi(u.x), bf_lo(u.y), bf_hi(u.y));
+}
+
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// All the unit's state blocks into `dst` (a 1024-byte aligned stage).
+template <typename StateT>
+__device__ __forceinline__ void tma_load_state(unsigned char* dst, const CUtensorMap* map, int h, int slot,
+                                               uint64_t* bar) {
+  using C = SwzCfg<StateT>;
+#pragma unroll
+  for (int blk = 0; blk < C::NBLK; ++blk) tma_load_3d(dst + blk * C::BLK_BYTES, map, blk * C::BLK_COLS, h * kD, slot, bar);
+}
+
+// Named barrier `id` over `nthreads` threads with an AND vote of `ok`.
+__device__ __forceinline__ bool bar_and(int id, int nthreads, bool ok) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)ok), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// ---- host side -----------------------------------------------------------------------
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+// The pool [num_slots][H*128 rows][128 columns] as a 3-d tensor map whose box
+// is one 128-byte-wide column block of one (slot, head) state.
+template <typename StateT>
+inline bool encode_state_map(CUtensorMap* map, void* state, int H, int num_slots, int64_t slot_stride) {
+  EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr) return false;
+  using C = SwzCfg<StateT>;
+  const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H * kD, (cuuint64_t)num_slots};
+  const cuuint64_t strides[2] = {(cuuint64_t)kD * sizeof(StateT), (cuuint64_t)slot_stride * sizeof(StateT)};
+  const cuuint32_t box[3] = {(cuuint32_t)C::BLK_COLS, (cuuint32_t)kD, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, sizeof(StateT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, state,
+             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace kda

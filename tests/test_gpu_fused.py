@@ -122,3 +122,67 @@ def test_fused_graph_replay_with_null_rows():
     g.replay()
     torch.cuda.synchronize()
     _check(c2, d, before, cbefore, out)
+
+
+# ---- persistent streaming schedule -------------------------------------------------
+
+@pytest.fixture
+def stream_schedule():
+    binding.kda_set_schedule_override(binding.SCHED_STREAM)
+    yield
+    binding.kda_set_schedule_override(binding.SCHED_AUTO)
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("lower_bound", [-5.0, None])
+@pytest.mark.parametrize("H,rows", [(8, 3), (12, 40), (32, 64)])
+def test_fused_stream_parity(stream_schedule, state_dtype, lower_bound, H, rows):
+    case = synth.fused_case(H, rows, seed=H + rows, state_dtype=state_dtype, null_frac=0.2)
+    d = _device_case(case)
+    before, cbefore = d["state"].clone(), d["conv_state"].clone()
+    out = torch.full((1, rows, H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    _run(d, lower_bound=lower_bound, out=out)
+    torch.cuda.synchronize()
+    sample = None if rows * H <= 1024 else sorted(np.random.default_rng(3).choice(rows, 24, replace=False).tolist())
+    _check(case, d, before, cbefore, out, rows=sample, lower_bound=lower_bound)
+    assert binding.kda_device_error() == 0
+
+
+def test_fused_stream_many_units_and_graph(stream_schedule):
+    """Many rounds through every stage, under graph replay with new inputs."""
+    H, rows = 8, 300
+    c1 = synth.fused_case(H, rows, seed=31, null_frac=0.1)
+    d = _device_case(c1)
+    out = torch.empty(1, rows, H, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run(d, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _run(d, out=out)
+    c2 = synth.fused_case(H, rows, seed=32, null_frac=0.15)
+    for key in ("x", "raw_gate", "raw_beta", "output_gate", "state_indices", "state"):
+        d[key].copy_(c2[key].cuda())
+    d["conv_state"].copy_(c2["conv_state"].cuda())
+    c2["conv_weight"], c2["A_log"], c2["dt_bias"], c2["norm_weight"] = (
+        c1["conv_weight"], c1["A_log"], c1["dt_bias"], c1["norm_weight"])
+    before, cbefore = d["state"].clone(), d["conv_state"].clone()
+    g.replay()
+    torch.cuda.synchronize()
+    rows_s = sorted(np.random.default_rng(4).choice(rows, 40, replace=False).tolist())
+    _check(c2, d, before, cbefore, out, rows=rows_s)
+    assert binding.kda_device_error() == 0
+
+
+def test_fused_stream_rejects_unaligned_rows(stream_schedule):
+    H, rows = 8, 4
+    case = synth.fused_case(H, rows, seed=33)
+    d = _device_case(case)
+    wide = torch.zeros(rows, 3 * H * 128 + 4, dtype=torch.bfloat16, device="cuda")
+    wide[:, : 3 * H * 128] = d["x"]
+    d["x"] = wide[:, : 3 * H * 128]
+    with pytest.raises(binding.KdaError) as e:
+        _run(d)
+    assert e.value.status == 2

@@ -96,8 +96,13 @@ def test_spec_precomputed_beta():
     _check(case, d, before, out, beta_is_logit=False)
 
 
-def test_spec_equals_sequential_single_token_calls():
-    """One T-token call == T calls of one token per row (fp32 state: bitwise)."""
+@pytest.mark.parametrize("split", [8, 0])
+def test_spec_equals_sequential_single_token_calls(split):
+    """One T-token call == T calls of one token per row: bitwise for fp32 state
+    under one kernel configuration (split 8 here), within the fp32 state and
+    output tolerances under the policy, which may pick another split for the
+    smaller single-token calls (a different shuffle-reduction order)."""
+    binding.kda_set_split_override(split)
     case = synth.spec_case(12, 6, seed=5, H=16)
     lens, cu = case["lengths"], case["cu_seqlens"]
     d = P.to_device(case)
@@ -114,8 +119,13 @@ def test_spec_equals_sequential_single_token_calls():
         o = _run(sub, 1)
         out_seq[tok.cuda()] = o
     torch.cuda.synchronize()
-    assert torch.equal(d["state"], d2["state"])
-    assert torch.equal(out_all, out_seq)
+    binding.kda_set_split_override(0)
+    if split:
+        assert torch.equal(d["state"], d2["state"])
+        assert torch.equal(out_all, out_seq)
+    else:
+        assert (d["state"] - d2["state"]).abs().max().item() <= P.F32_STATE_ATOL
+        assert (out_all.float() - out_seq.float()).abs().max().item() <= P.OUT_ATOL
 
 
 def test_spec_trailing_empty_rows_golden():
