@@ -219,7 +219,7 @@ def make_workload(args, seed):
     if args.workload == "packed":
         return Packed(B=args.batch or 512, slots=args.slots or 2048, seed=seed)
     if args.workload == "fused":
-        return Fused(H=args.heads or 32, rows=args.batch or 256, slots=args.slots, seed=seed)
+        return Fused(H=args.heads or 32, rows=args.batch or 256, slots=args.slots or None, seed=seed)
     return Spec(N=args.batch or 128, t_max=args.t_max or 6, H=args.heads or 16, slots=args.slots, seed=seed)
 
 

@@ -265,6 +265,7 @@ int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   const int forced = g_schedule_override.load();
   if (forced != KDA_SCHED_AUTO) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
+  if (op == KDA_OP_FUSED) return KDA_SCHED_SPLIT;  // the split kernel measured faster for fused
   // Measured on GB300 (152 SMs): the streaming kernel wins from about five
   // units per SM (Kimi-Linear H=32 B>=24, packed K3 B>=64).
   return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
@@ -286,7 +287,9 @@ int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   if (forced != 0) return forced;
   // Measured on GB300 for the split kernel (used below the streaming
   // threshold): 16 value slabs per unit while the units are fewer than half
-  // the SMs, 8 above.  Longer speculative rows keep 8 as well.
+  // the SMs, 8 above.  Speculative rows carry T tokens of work per state
+  // block: there 2 slabs per unit win once the units reach the SM count.
+  if (op == KDA_OP_SPEC && units >= sms) return 2;
   return 2 * units <= sms ? 16 : 8;
 }
 

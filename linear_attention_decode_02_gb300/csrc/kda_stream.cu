@@ -6,7 +6,7 @@
 //                  in 128-byte-wide column blocks) and bulk copies of the
 //                  unit's activation vectors, all completing on the stage's
 //                  `full` barrier.
-//   prologue warp  per unit, once: (fused: the short conv + SiLU of the
+//   prologue warps per unit, once, units dealt round-robin: (fused: the short conv + SiLU of the
 //                  head's 384 channels and the conv-cache shift) the L2 norms,
 //                  gate and decay of the 128 key channels into the stage's
 //                  coefficient array (d k, d q, d, k) and q.k; then `ready`.
@@ -37,6 +37,10 @@ constexpr uint32_t T1_ACT_SLOT = 512;  // one 128-vector, up to float32: q, k, v
 
 template <typename StateT>
 using T1Stream = StageCfg<StateT, 5 * T1_ACT_SLOT, sizeof(StateT) == 4 ? 3 : 5>;
+// Prologue warps.  Units are dealt to them round-robin; NP must divide
+// NSTAGE so each stage is always served by the same prologue warp in round
+// order (a parity wait cannot tell a phase from the one two rounds later).
+constexpr int T1_NP = 1;
 
 template <typename StateT>
 __host__ __device__ constexpr size_t t1_stream_smem() {
@@ -44,11 +48,12 @@ __host__ __device__ constexpr size_t t1_stream_smem() {
 }
 
 template <typename StateT>
-__global__ void __launch_bounds__((T1Stream<StateT>::NW + 2) * 32, 1)
+__global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     kda_t1_stream_kernel(const T1Args a, const __grid_constant__ CUtensorMap state_map, const int units) {
   using C = T1Stream<StateT>;
   using G = Strip<StateT, C::CW>;
   static_assert(t1_stream_smem<StateT>() <= 232448, "stages exceed the 227 KB shared memory of a CTA");
+  static_assert(C::NSTAGE % T1_NP == 0, "each stage must be served by one prologue warp");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -130,9 +135,9 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 2) * 32, 1)
     return;
   }
 
-  if (warp == C::NW + 1) {
-    // ---------------- prologue: the unit's per-key-channel coefficients, once ----------------
-    for (int j = 0; j < n_my; ++j) {
+  if (warp > C::NW) {
+    // ---------------- prologue warps (units round-robin): per-key-channel coefficients, once ----------------
+    for (int j = warp - C::NW - 1; j < n_my; j += T1_NP) {
       const int s = j % C::NSTAGE;
       const bool ok = mbar_wait(&full[s], (j / C::NSTAGE) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -249,7 +254,12 @@ constexpr uint32_t F_X = 0, F_CS = 768, F_G = 3072, F_DT = 3328, F_OG = 3840, F_
 constexpr uint32_t F_DERIVED = 3 * kD * sizeof(float);  // SiLU(conv) of the 384 channels
 
 template <typename StateT>
-using FusedStream = StageCfg<StateT, F_ACT, sizeof(StateT) == 4 ? 3 : 5, F_DERIVED>;
+using FusedStream = StageCfg<StateT, F_ACT, sizeof(StateT) == 4 ? 3 : 4, F_DERIVED>;
+// Prologue warps (the short conv dominates their work); NP divides NSTAGE.
+template <typename StateT>
+__host__ __device__ constexpr int fused_np() {
+  return sizeof(StateT) == 4 ? 3 : 2;
+}
 
 template <typename StateT>
 __host__ __device__ constexpr size_t fused_stream_smem() {
@@ -257,11 +267,12 @@ __host__ __device__ constexpr size_t fused_stream_smem() {
 }
 
 template <typename StateT>
-__global__ void __launch_bounds__((FusedStream<StateT>::NW + 2) * 32, 1)
+__global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT>()) * 32, 1)
     kda_fused_stream_kernel(const FusedArgs a, const __grid_constant__ CUtensorMap state_map, const int units) {
   using C = FusedStream<StateT>;
   using G = Strip<StateT, C::CW>;
   static_assert(fused_stream_smem<StateT>() <= 232448, "stages exceed the 227 KB shared memory of a CTA");
+  static_assert(C::NSTAGE % fused_np<StateT>() == 0, "each stage must be served by one prologue warp");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -351,9 +362,9 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 2) * 32, 1)
     return;
   }
 
-  if (warp == C::NW + 1) {
-    // ---------------- prologue: conv + SiLU, cache shift, coefficients ----------------
-    for (int j = 0; j < n_my; ++j) {
+  if (warp > C::NW) {
+    // ---------------- prologue warps (units round-robin): conv + SiLU, cache shift, coefficients ----------------
+    for (int j = warp - C::NW - 1; j < n_my; j += fused_np<StateT>()) {
       const int s = j % C::NSTAGE;
       const bool ok = mbar_wait(&full[s], (j / C::NSTAGE) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -537,7 +548,7 @@ cudaError_t launch_t1_stream_typed(const T1Args& a, int sm_count, cudaStream_t s
   if (e != cudaSuccess) return e;
   const int units = a.B * a.H;
   const int grid = units < sm_count ? units : sm_count;
-  kda_t1_stream_kernel<StateT><<<grid, (T1Stream<StateT>::NW + 2) * 32, smem, s>>>(a, map, units);
+  kda_t1_stream_kernel<StateT><<<grid, (T1Stream<StateT>::NW + 1 + T1_NP) * 32, smem, s>>>(a, map, units);
   return cudaGetLastError();
 }
 
@@ -551,7 +562,8 @@ cudaError_t launch_fused_stream_typed(const FusedArgs& a, int sm_count, cudaStre
   if (e != cudaSuccess) return e;
   const int units = a.rows * a.H;
   const int grid = units < sm_count ? units : sm_count;
-  kda_fused_stream_kernel<StateT><<<grid, (FusedStream<StateT>::NW + 2) * 32, smem, s>>>(a, map, units);
+  kda_fused_stream_kernel<StateT><<<grid, (FusedStream<StateT>::NW + 1 + fused_np<StateT>()) * 32, smem, s>>>(
+      a, map, units);
   return cudaGetLastError();
 }
 

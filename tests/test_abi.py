@@ -48,6 +48,8 @@ def test_plan_split_policy(lib):
     assert binding.kda_plan_split(0, 32, 0, 1, 152) == 16
     assert binding.kda_plan_split(0, 76, 0, 1, 152) == 16
     assert binding.kda_plan_split(0, 77, 0, 1, 152) == 8
+    assert binding.kda_plan_split(3, 2048, 0, 6, 152) == 2  # long speculative rows
+    assert binding.kda_plan_split(3, 100, 0, 6, 152) == 8
     assert binding.kda_plan_split(2, 8, 0, 1, 152) == 1  # fused is always split 1
     assert binding.kda_plan_split(0, 1, 5, 1, 152) == 0  # bad dtype
     assert binding.kda_plan_split(9, 1, 0, 1, 152) == 0  # bad op
