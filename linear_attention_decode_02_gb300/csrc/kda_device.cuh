@@ -47,6 +47,13 @@ struct Frag<float> {
   __device__ __forceinline__ static Raw pack(const float (&s)[VEC]) {
     return make_float4(s[0], s[1], s[2], s[3]);
   }
+  // Column pair p (elements 2p, 2p+1) as float2, and back.
+  __device__ __forceinline__ static float2 get2(const Raw& r, int p) {
+    return p == 0 ? make_float2(r.x, r.y) : make_float2(r.z, r.w);
+  }
+  __device__ __forceinline__ static Raw pack2(const float2 (&y)[VEC / 2]) {
+    return make_float4(y[0].x, y[0].y, y[1].x, y[1].y);
+  }
 };
 
 template <>
@@ -67,7 +74,22 @@ struct Frag<__nv_bfloat16> {
     return make_uint4(pack_bf2(s[0], s[1]), pack_bf2(s[2], s[3]), pack_bf2(s[4], s[5]),
                       pack_bf2(s[6], s[7]));
   }
+  __device__ __forceinline__ static float2 get2(const Raw& r, int p) {
+    const uint32_t w = p == 0 ? r.x : (p == 1 ? r.y : (p == 2 ? r.z : r.w));
+    return make_float2(bf_lo(w), bf_hi(w));
+  }
+  __device__ __forceinline__ static Raw pack2(const float2 (&y)[VEC / 2]) {
+    return make_uint4(pack_bf2(y[0].x, y[0].y), pack_bf2(y[1].x, y[1].y), pack_bf2(y[2].x, y[2].y),
+                      pack_bf2(y[3].x, y[3].y));
+  }
 };
+
+// Paired float32 arithmetic (one instruction for two lanes' worth of
+// columns); every component is rounded exactly like the scalar operation.
+__device__ __forceinline__ float2 dup2(float x) { return make_float2(x, x); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 
 // Geometry of one warp's column strip: CW value columns x all 128 key rows.
 // Lanes walk a row segment with 16-byte vectors; a warp instruction covers

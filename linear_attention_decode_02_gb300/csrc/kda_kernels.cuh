@@ -55,17 +55,18 @@ __device__ __forceinline__ void load_cols(const void* base, int64_t i, int dtype
 
 // The lane's state fragments in two register forms: Raw keeps the stored
 // bytes (T=1: one read, one write, bf16 stays packed); Flt keeps float32
-// values across the tokens of a speculative row (one rounding at the end).
+// column pairs across the tokens of a speculative row (one rounding at the
+// end).  at2(i, p) is column pair p of fragment i.
 template <typename StateT, typename G>
 struct RawRegs {
   typename Frag<StateT>::Raw r[G::PASSES];
-  __device__ __forceinline__ float at(int i, int j) const { return Frag<StateT>::get(r[i], j); }
+  __device__ __forceinline__ float2 at2(int i, int p) const { return Frag<StateT>::get2(r[i], p); }
 };
 
 template <typename G>
 struct FltRegs {
-  float s[G::PASSES][G::VEC];
-  __device__ __forceinline__ float at(int i, int j) const { return s[i][j]; }
+  float2 s[G::PASSES][G::VEC / 2];
+  __device__ __forceinline__ float2 at2(int i, int p) const { return s[i][p]; }
 };
 
 template <typename StateT, typename G>
@@ -80,66 +81,112 @@ __device__ __forceinline__ void strip_load(const StateT* sp, int row0, int col0,
   for (int i = 0; i < G::PASSES; ++i) {
     const typename Frag<StateT>::Raw r = Frag<StateT>::load(sp + (row0 + i * G::RPI) * kD + col0);
 #pragma unroll
-    for (int j = 0; j < G::VEC; ++j) F.s[i][j] = Frag<StateT>::get(r, j);
+    for (int p = 0; p < G::VEC / 2; ++p) F.s[i][p] = Frag<StateT>::get2(r, p);
   }
 }
 
-// k-reduction of one token over the lane's fragments, completed across the
-// lanes that share the lane's columns (xor over the row-lane bits).
-template <typename G, typename Regs>
-__device__ __forceinline__ void strip_reduce(const Regs& S, const float4* coef, int row0,
-                                             float (&acc_a)[G::VEC], float (&acc_b)[G::VEC]) {
+// Accumulates one fragment row into the column-pair sums:
+// a += (d k)_row * S[row][cols], b += (d q)_row * S[row][cols].
+template <int NP2>
+__device__ __forceinline__ void accumulate_row(const float4& c, const float2* x2, float2 (&acc_a)[NP2],
+                                               float2 (&acc_b)[NP2]) {
+  const float2 ca = dup2(c.x), cb = dup2(c.y);
 #pragma unroll
-  for (int j = 0; j < G::VEC; ++j) { acc_a[j] = 0.f; acc_b[j] = 0.f; }
-#pragma unroll
-  for (int i = 0; i < G::PASSES; ++i) {
-    const float4 c = coef[row0 + i * G::RPI];
-#pragma unroll
-    for (int j = 0; j < G::VEC; ++j) {
-      const float x = S.at(i, j);
-      acc_a[j] = fmaf(c.x, x, acc_a[j]);
-      acc_b[j] = fmaf(c.y, x, acc_b[j]);
-    }
+  for (int p = 0; p < NP2; ++p) {
+    acc_a[p] = fma2(ca, x2[p], acc_a[p]);
+    acc_b[p] = fma2(cb, x2[p], acc_b[p]);
   }
+}
+
+// Completes the column sums across the lanes that share the lane's columns
+// (xor over the row-lane bits) and returns them as scalars.
+template <typename G>
+__device__ __forceinline__ void strip_allreduce(float2 (&acc_a)[G::VEC / 2], float2 (&acc_b)[G::VEC / 2],
+                                                float (&a)[G::VEC], float (&b)[G::VEC]) {
 #pragma unroll
   for (int o = G::LPR; o < 32; o <<= 1) {
 #pragma unroll
-    for (int j = 0; j < G::VEC; ++j) {
-      acc_a[j] += __shfl_xor_sync(0xffffffffu, acc_a[j], o);
-      acc_b[j] += __shfl_xor_sync(0xffffffffu, acc_b[j], o);
+    for (int p = 0; p < G::VEC / 2; ++p) {
+      acc_a[p] = add2(acc_a[p], make_float2(__shfl_xor_sync(0xffffffffu, acc_a[p].x, o),
+                                            __shfl_xor_sync(0xffffffffu, acc_a[p].y, o)));
+      acc_b[p] = add2(acc_b[p], make_float2(__shfl_xor_sync(0xffffffffu, acc_b[p].x, o),
+                                            __shfl_xor_sync(0xffffffffu, acc_b[p].y, o)));
     }
+  }
+#pragma unroll
+  for (int p = 0; p < G::VEC / 2; ++p) {
+    a[2 * p] = acc_a[p].x; a[2 * p + 1] = acc_a[p].y;
+    b[2 * p] = acc_b[p].x; b[2 * p + 1] = acc_b[p].y;
   }
 }
 
-// S'[k][v] = d_k S[k][v] + k_k u_v, written straight back (T=1).
+// k-reduction of one token over the lane's fragments: a_v = sum_k (d k)_k S[k][v],
+// b_v = sum_k (d q)_k S[k][v] for the lane's VEC columns.
+template <typename G, typename Regs>
+__device__ __forceinline__ void strip_reduce(const Regs& S, const float4* coef, int row0, float (&acc_a)[G::VEC],
+                                             float (&acc_b)[G::VEC]) {
+  float2 a2[G::VEC / 2], b2[G::VEC / 2];
+#pragma unroll
+  for (int p = 0; p < G::VEC / 2; ++p) { a2[p] = make_float2(0.f, 0.f); b2[p] = make_float2(0.f, 0.f); }
+#pragma unroll
+  for (int i = 0; i < G::PASSES; ++i) {
+    float2 x2[G::VEC / 2];
+#pragma unroll
+    for (int p = 0; p < G::VEC / 2; ++p) x2[p] = S.at2(i, p);
+    accumulate_row<G::VEC / 2>(coef[row0 + i * G::RPI], x2, a2, b2);
+  }
+  strip_allreduce<G>(a2, b2, acc_a, acc_b);
+}
+
+// Column pairs of u for the paired update.
+template <int VEC>
+__device__ __forceinline__ void pairs_of(const float (&u)[VEC], float2 (&u2)[VEC / 2]) {
+#pragma unroll
+  for (int p = 0; p < VEC / 2; ++p) u2[p] = make_float2(u[2 * p], u[2 * p + 1]);
+}
+
+// S'[k][v] = d_k S[k][v] + k_k u_v for one fragment row (decay d, key k).
+template <int NP2>
+__device__ __forceinline__ void update_row(float d, float k, const float2* x2, const float2 (&u2)[NP2],
+                                           float2 (&y2)[NP2]) {
+  const float2 dd = dup2(d), kk = dup2(k);
+#pragma unroll
+  for (int p = 0; p < NP2; ++p) y2[p] = fma2(dd, x2[p], mul2(kk, u2[p]));
+}
+
+// S' = d S + k u^T, written straight back (T=1).
 template <typename StateT, typename G>
 __device__ __forceinline__ void strip_update_store(StateT* sp, int row0, int col0, const RawRegs<StateT, G>& R,
                                                    const float4* coef, const float (&u)[G::VEC]) {
+  float2 u2[G::VEC / 2];
+  pairs_of<G::VEC>(u, u2);
 #pragma unroll
   for (int i = 0; i < G::PASSES; ++i) {
     const float4 c = coef[row0 + i * G::RPI];
-    float y[G::VEC];
+    float2 x2[G::VEC / 2], y2[G::VEC / 2];
 #pragma unroll
-    for (int j = 0; j < G::VEC; ++j) y[j] = fmaf(c.z, R.at(i, j), c.w * u[j]);
-    Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack(y));
+    for (int p = 0; p < G::VEC / 2; ++p) x2[p] = R.at2(i, p);
+    update_row<G::VEC / 2>(c.z, c.w, x2, u2, y2);
+    Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(y2));
   }
 }
 
 // Same update kept in float registers (speculative token loop).
 template <typename G>
 __device__ __forceinline__ void strip_update(FltRegs<G>& F, const float4* coef, int row0, const float (&u)[G::VEC]) {
+  float2 u2[G::VEC / 2];
+  pairs_of<G::VEC>(u, u2);
 #pragma unroll
   for (int i = 0; i < G::PASSES; ++i) {
     const float4 c = coef[row0 + i * G::RPI];
-#pragma unroll
-    for (int j = 0; j < G::VEC; ++j) F.s[i][j] = fmaf(c.z, F.s[i][j], c.w * u[j]);
+    update_row<G::VEC / 2>(c.z, c.w, F.s[i], u2, F.s[i]);
   }
 }
 
 template <typename StateT, typename G>
 __device__ __forceinline__ void strip_store(StateT* sp, int row0, int col0, const FltRegs<G>& F) {
 #pragma unroll
-  for (int i = 0; i < G::PASSES; ++i) Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack(F.s[i]));
+  for (int i = 0; i < G::PASSES; ++i) Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(F.s[i]));
 }
 
 // Minimum resident CTAs per SM for a CTA of NW warps: keeps >= 16 warps per

@@ -30,6 +30,45 @@ __device__ unsigned int g_kda_device_error = 0;
 
 __device__ __forceinline__ void record_error(unsigned int bit) { atomicOr(&g_kda_device_error, bit); }
 
+// Consumer core shared by the stream kernels: reads the lane's fragments of
+// a swizzled stage into registers, keeps each row's (decay, key) pair, and
+// accumulates the column-pair sums of the two k-reductions.
+template <typename StateT, typename G>
+__device__ __forceinline__ void reduce_stage(const unsigned char* st, const float4* coef, int row0, int col0,
+                                             typename Frag<StateT>::Raw (&S)[G::PASSES], float2 (&dk)[G::PASSES],
+                                             float2 (&acc_a)[G::VEC / 2], float2 (&acc_b)[G::VEC / 2]) {
+#pragma unroll
+  for (int p = 0; p < G::VEC / 2; ++p) { acc_a[p] = make_float2(0.f, 0.f); acc_b[p] = make_float2(0.f, 0.f); }
+#pragma unroll
+  for (int i = 0; i < G::PASSES; ++i) {
+    const int r = row0 + i * G::RPI;
+    S[i] = *reinterpret_cast<const typename Frag<StateT>::Raw*>(st + swz_offset<StateT>(r, col0));
+    const float4 c = coef[r];
+    dk[i] = make_float2(c.z, c.w);
+    float2 x2[G::VEC / 2];
+#pragma unroll
+    for (int p = 0; p < G::VEC / 2; ++p) x2[p] = Frag<StateT>::get2(S[i], p);
+    accumulate_row<G::VEC / 2>(c, x2, acc_a, acc_b);
+  }
+}
+
+// S' = d S + k u^T from the registers of reduce_stage, stored to global.
+template <typename StateT, typename G>
+__device__ __forceinline__ void update_store_regs(StateT* sp, int row0, int col0,
+                                                  const typename Frag<StateT>::Raw (&S)[G::PASSES],
+                                                  const float2 (&dk)[G::PASSES], const float (&u)[G::VEC]) {
+  float2 u2[G::VEC / 2];
+  pairs_of<G::VEC>(u, u2);
+#pragma unroll
+  for (int i = 0; i < G::PASSES; ++i) {
+    float2 x2[G::VEC / 2], y2[G::VEC / 2];
+#pragma unroll
+    for (int p = 0; p < G::VEC / 2; ++p) x2[p] = Frag<StateT>::get2(S[i], p);
+    update_row<G::VEC / 2>(dk[i].x, dk[i].y, x2, u2, y2);
+    Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(y2));
+  }
+}
+
 // =====================================================================================
 // T=1 recurrent / packed
 // =====================================================================================
@@ -189,6 +228,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     }
     const unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
     const float4* coef = coef_all + s * kD;
+    float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
     float vv[G::VEC];
 #pragma unroll
     for (int jj = 0; jj < G::VEC; jj += 4) {
@@ -198,32 +238,11 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     // k-reductions; the decay and key coefficients of each row stay in registers
     typename Frag<StateT>::Raw S[G::PASSES];
     float2 dk[G::PASSES];
-    float acc_a[G::VEC], acc_b[G::VEC];
-#pragma unroll
-    for (int jj = 0; jj < G::VEC; ++jj) { acc_a[jj] = 0.f; acc_b[jj] = 0.f; }
-#pragma unroll
-    for (int i = 0; i < G::PASSES; ++i) {
-      const int r = row0 + i * G::RPI;
-      S[i] = *reinterpret_cast<const typename Frag<StateT>::Raw*>(st + swz_offset<StateT>(r, col0));
-      const float4 c = coef[r];
-      dk[i] = make_float2(c.z, c.w);
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) {
-        const float x = Frag<StateT>::get(S[i], jj);
-        acc_a[jj] = fmaf(c.x, x, acc_a[jj]);
-        acc_b[jj] = fmaf(c.y, x, acc_b[jj]);
-      }
-    }
+    reduce_stage<StateT, G>(st, coef, row0, col0, S, dk, acc2_a, acc2_b);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the stage
-#pragma unroll
-    for (int o = G::LPR; o < 32; o <<= 1) {
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) {
-        acc_a[jj] += __shfl_xor_sync(0xffffffffu, acc_a[jj], o);
-        acc_b[jj] += __shfl_xor_sync(0xffffffffu, acc_b[jj], o);
-      }
-    }
+    float acc_a[G::VEC], acc_b[G::VEC];
+    strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
     const float beta = __int_as_float(sc.y);
     const float qk = __int_as_float(sc.w);
     float u_[G::VEC], o[G::VEC];
@@ -233,13 +252,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       o[jj] = a.scale * (acc_b[jj] + qk * u_[jj]);
     }
     StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
-#pragma unroll
-    for (int i = 0; i < G::PASSES; ++i) {
-      float y[G::VEC];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) y[jj] = fmaf(dk[i].x, Frag<StateT>::get(S[i], jj), dk[i].y * u_[jj]);
-      Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack(y));
-    }
+    update_store_regs<StateT, G>(sp, row0, col0, S, dk, u_);
     if (row0 == 0) store_out<G::VEC>(out + col0, o);
   }
 }
@@ -450,32 +463,12 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
       }
       typename Frag<StateT>::Raw S[G::PASSES];
       float2 dk[G::PASSES];
-      float acc_a[G::VEC], acc_b[G::VEC];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) { acc_a[jj] = 0.f; acc_b[jj] = 0.f; }
-#pragma unroll
-      for (int i = 0; i < G::PASSES; ++i) {
-        const int rr = row0 + i * G::RPI;
-        S[i] = *reinterpret_cast<const typename Frag<StateT>::Raw*>(st + swz_offset<StateT>(rr, col0));
-        const float4 c = coef[rr];
-        dk[i] = make_float2(c.z, c.w);
-#pragma unroll
-        for (int jj = 0; jj < G::VEC; ++jj) {
-          const float x = Frag<StateT>::get(S[i], jj);
-          acc_a[jj] = fmaf(c.x, x, acc_a[jj]);
-          acc_b[jj] = fmaf(c.y, x, acc_b[jj]);
-        }
-      }
+      float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
+      reduce_stage<StateT, G>(st, coef, row0, col0, S, dk, acc2_a, acc2_b);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
-#pragma unroll
-      for (int sh = G::LPR; sh < 32; sh <<= 1) {
-#pragma unroll
-        for (int jj = 0; jj < G::VEC; ++jj) {
-          acc_a[jj] += __shfl_xor_sync(0xffffffffu, acc_a[jj], sh);
-          acc_b[jj] += __shfl_xor_sync(0xffffffffu, acc_b[jj], sh);
-        }
-      }
+      float acc_a[G::VEC], acc_b[G::VEC];
+      strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
       const float beta = __int_as_float(sc.y);
       const float qk = __int_as_float(sc.w);
       float u_[G::VEC];
@@ -486,13 +479,7 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         ss = fmaf(o[jj], o[jj], ss);
       }
       StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
-#pragma unroll
-      for (int i = 0; i < G::PASSES; ++i) {
-        float y[G::VEC];
-#pragma unroll
-        for (int jj = 0; jj < G::VEC; ++jj) y[jj] = fmaf(dk[i].x, Frag<StateT>::get(S[i], jj), dk[i].y * u_[jj]);
-        Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack(y));
-      }
+      update_store_regs<StateT, G>(sp, row0, col0, S, dk, u_);
     } else if (ok) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
