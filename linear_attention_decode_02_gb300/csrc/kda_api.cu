@@ -256,18 +256,22 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
   return KDA_OK;
 }
 
-// T=1 schedule: the persistent streaming kernel once the units fill several
-// waves of the SMs, the split kernel below that (latency-bound sizes).
+// Schedule policy, measured on GB300 (152 SMs) with CUDA-graph timings and
+// an L2 flush between replays:
+//  - float32 state, T=1: the split kernel (4 value slabs per unit) reaches
+//    ~95% of copy bandwidth at B >= 128 and beats the streaming kernel;
+//  - bfloat16 state, T=1: the streaming kernel once the units fill five per
+//    SM (packed K3 B >= 64), the split kernel below;
+//  - fused: the streaming kernel from sixteen units per SM, split below;
+//  - speculative rows: the split kernel.
 int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
-  (void)state_dtype;
   (void)t_max;
   if (op == KDA_OP_SPEC) return KDA_SCHED_SPLIT;
   const int forced = g_schedule_override.load();
   if (forced != KDA_SCHED_AUTO) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
-  if (op == KDA_OP_FUSED) return KDA_SCHED_SPLIT;  // the split kernel measured faster for fused
-  // Measured on GB300 (152 SMs): the streaming kernel wins from about five
-  // units per SM (Kimi-Linear H=32 B>=24, packed K3 B>=64).
+  if (op == KDA_OP_FUSED) return units >= 16LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
+  if (state_dtype == KDA_F32) return KDA_SCHED_SPLIT;
   return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
 }
 
@@ -285,11 +289,12 @@ int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   const int forced = g_split_override.load();
   if (op == KDA_OP_FUSED) return 1;
   if (forced != 0) return forced;
-  // Measured on GB300 for the split kernel (used below the streaming
-  // threshold): 16 value slabs per unit while the units are fewer than half
-  // the SMs, 8 above.  Speculative rows carry T tokens of work per state
-  // block: there 2 slabs per unit win once the units reach the SM count.
-  if (op == KDA_OP_SPEC && units >= sms) return 2;
+  // Measured on GB300 for the split kernel: speculative rows (T tokens of
+  // work per state block) 2 value slabs per unit at every size; T=1 with
+  // the units at five or more per SM 4 slabs, fewer than half the SM count
+  // 16 slabs, 8 in between.
+  if (op == KDA_OP_SPEC) return 2;
+  if (units >= 5LL * sms) return 4;
   return 2 * units <= sms ? 16 : 8;
 }
 

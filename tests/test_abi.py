@@ -43,13 +43,16 @@ def test_status_strings_and_version(lib):
 
 
 def test_plan_split_policy(lib):
-    # split kernel: 16 slabs per unit below half the SM count, 8 above
-    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 8
+    # split kernel: 16 slabs per unit below half the SM count, 8 up to five
+    # units per SM, 4 above; speculative rows always 2
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
     assert binding.kda_plan_split(0, 32, 0, 1, 152) == 16
     assert binding.kda_plan_split(0, 76, 0, 1, 152) == 16
     assert binding.kda_plan_split(0, 77, 0, 1, 152) == 8
-    assert binding.kda_plan_split(3, 2048, 0, 6, 152) == 2  # long speculative rows
-    assert binding.kda_plan_split(3, 100, 0, 6, 152) == 8
+    assert binding.kda_plan_split(0, 759, 0, 1, 152) == 8
+    assert binding.kda_plan_split(0, 760, 0, 1, 152) == 4
+    assert binding.kda_plan_split(3, 2048, 0, 6, 152) == 2
+    assert binding.kda_plan_split(3, 16, 0, 6, 152) == 2
     assert binding.kda_plan_split(2, 8, 0, 1, 152) == 1  # fused is always split 1
     assert binding.kda_plan_split(0, 1, 5, 1, 152) == 0  # bad dtype
     assert binding.kda_plan_split(9, 1, 0, 1, 152) == 0  # bad op
@@ -64,7 +67,7 @@ def test_split_override(lib):
     assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
     assert binding.kda_plan_split(2, 16384, 0, 1, 152) == 1
     assert lib.kda_set_split_override(0) == OK
-    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 8
+    assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
 
 
 def _recurrent_args(B=2, H=2, N=4, qkv=torch.bfloat16, state=torch.float32):
@@ -260,8 +263,12 @@ def test_schedule_override_and_plan(lib):
     assert binding.kda_plan_schedule(0, 1, 0, 1, 152) == 2
     assert binding.kda_plan_schedule(3, 1, 0, 1, 152) == 1  # spec has one schedule
     assert lib.kda_set_schedule_override(0) == OK
-    assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 2
+    assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 2  # bf16 packed: stream
     assert binding.kda_plan_schedule(1, 12, 1, 1, 152) == 1
+    assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == 1  # fp32: split kernel
+    assert binding.kda_plan_schedule(0, 16384, 1, 1, 152) == 2  # bf16 state: stream
+    assert binding.kda_plan_schedule(2, 8192, 0, 1, 152) == 2  # fused, many units
+    assert binding.kda_plan_schedule(2, 1024, 0, 1, 152) == 1
     assert lib.kda_set_split_override(8) == OK  # a forced split implies the split schedule
     assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 1
     assert lib.kda_set_split_override(0) == OK

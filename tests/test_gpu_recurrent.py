@@ -333,9 +333,10 @@ def test_packed_stream_schedule(stream_schedule, B):
 
 
 def test_schedule_policy_queries():
-    assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == binding.SCHED_STREAM
-    assert binding.kda_plan_schedule(0, 32, 0, 1, 152) == binding.SCHED_SPLIT
-    assert binding.kda_plan_schedule(2, 16384, 0, 1, 152) == binding.SCHED_SPLIT
+    assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == binding.SCHED_SPLIT
+    assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == binding.SCHED_STREAM
+    assert binding.kda_plan_schedule(0, 32, 1, 1, 152) == binding.SCHED_SPLIT
+    assert binding.kda_plan_schedule(2, 16384, 0, 1, 152) == binding.SCHED_STREAM
     assert binding.kda_plan_schedule(3, 16384, 0, 1, 152) == binding.SCHED_SPLIT
 
 
