@@ -147,14 +147,9 @@ __device__ __forceinline__ float log_decay(float x, float a, int gate_mode, floa
 
 __device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
 
-// Coefficients of key row r occupy coef[2r] = (d k, d k, d q, d q) and
-// coef[2r + 1] = (d, d, k, k): each float4 holds two ready-made pairs for
-// the paired float32 arithmetic.
-constexpr int kCoefPerRow = 2;
-
 // Per-lane prologue of one token for one head: lane l holds channels 4l..4l+3
-// of q, k and the decay d = exp(g).  Writes the coefficients of those rows
-// (k, q L2-normalised) and returns q_hat . k_hat (same on every lane).
+// of q, k and the decay d = exp(g).  Writes (d*k_hat, d*q_hat, d, k_hat) for
+// those channels to coef[] and returns q_hat . k_hat (same on every lane).
 __device__ __forceinline__ float token_coefficients(float4 q, float4 k, float4 d, int lane,
                                                     float4* coef) {
   float qq = q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
@@ -170,9 +165,7 @@ __device__ __forceinline__ float token_coefficients(float4 q, float4 k, float4 d
     const float kh = f4get(k, j) * rk;
     const float qh = f4get(q, j) * rq;
     const float dj = f4get(d, j);
-    const float dk = dj * kh, dq = dj * qh;
-    coef[kCoefPerRow * (4 * lane + j)] = make_float4(dk, dk, dq, dq);
-    coef[kCoefPerRow * (4 * lane + j) + 1] = make_float4(dj, dj, kh, kh);
+    coef[4 * lane + j] = make_float4(dj * kh, dj * qh, dj, kh);
   }
   return qk * rq * rk;
 }

@@ -86,12 +86,11 @@ __device__ __forceinline__ void strip_load(const StateT* sp, int row0, int col0,
 }
 
 // Accumulates one fragment row into the column-pair sums:
-// a += (d k)_row * S[row][cols], b += (d q)_row * S[row][cols];
-// c = (d k, d k, d q, d q) of the row.
+// a += (d k)_row * S[row][cols], b += (d q)_row * S[row][cols].
 template <int NP2>
 __device__ __forceinline__ void accumulate_row(const float4& c, const float2* x2, float2 (&acc_a)[NP2],
                                                float2 (&acc_b)[NP2]) {
-  const float2 ca = make_float2(c.x, c.y), cb = make_float2(c.z, c.w);
+  const float2 ca = dup2(c.x), cb = dup2(c.y);
 #pragma unroll
   for (int p = 0; p < NP2; ++p) {
     acc_a[p] = fma2(ca, x2[p], acc_a[p]);
@@ -134,7 +133,7 @@ __device__ __forceinline__ void strip_reduce(const Regs& S, const float4* coef, 
     float2 x2[G::VEC / 2];
 #pragma unroll
     for (int p = 0; p < G::VEC / 2; ++p) x2[p] = S.at2(i, p);
-    accumulate_row<G::VEC / 2>(coef[kCoefPerRow * (row0 + i * G::RPI)], x2, a2, b2);
+    accumulate_row<G::VEC / 2>(coef[row0 + i * G::RPI], x2, a2, b2);
   }
   strip_allreduce<G>(a2, b2, acc_a, acc_b);
 }
@@ -146,11 +145,11 @@ __device__ __forceinline__ void pairs_of(const float (&u)[VEC], float2 (&u2)[VEC
   for (int p = 0; p < VEC / 2; ++p) u2[p] = make_float2(u[2 * p], u[2 * p + 1]);
 }
 
-// S'[k][v] = d_k S[k][v] + k_k u_v for one fragment row; c = (d, d, k, k).
+// S'[k][v] = d_k S[k][v] + k_k u_v for one fragment row (decay d, key k).
 template <int NP2>
-__device__ __forceinline__ void update_row(const float4& c, const float2* x2, const float2 (&u2)[NP2],
+__device__ __forceinline__ void update_row(float d, float k, const float2* x2, const float2 (&u2)[NP2],
                                            float2 (&y2)[NP2]) {
-  const float2 dd = make_float2(c.x, c.y), kk = make_float2(c.z, c.w);
+  const float2 dd = dup2(d), kk = dup2(k);
 #pragma unroll
   for (int p = 0; p < NP2; ++p) y2[p] = fma2(dd, x2[p], mul2(kk, u2[p]));
 }
@@ -163,11 +162,11 @@ __device__ __forceinline__ void strip_update_store(StateT* sp, int row0, int col
   pairs_of<G::VEC>(u, u2);
 #pragma unroll
   for (int i = 0; i < G::PASSES; ++i) {
-    const float4 c = coef[kCoefPerRow * (row0 + i * G::RPI) + 1];
+    const float4 c = coef[row0 + i * G::RPI];
     float2 x2[G::VEC / 2], y2[G::VEC / 2];
 #pragma unroll
     for (int p = 0; p < G::VEC / 2; ++p) x2[p] = R.at2(i, p);
-    update_row<G::VEC / 2>(c, x2, u2, y2);
+    update_row<G::VEC / 2>(c.z, c.w, x2, u2, y2);
     Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(y2));
   }
 }
@@ -179,8 +178,8 @@ __device__ __forceinline__ void strip_update(FltRegs<G>& F, const float4* coef, 
   pairs_of<G::VEC>(u, u2);
 #pragma unroll
   for (int i = 0; i < G::PASSES; ++i) {
-    const float4 c = coef[kCoefPerRow * (row0 + i * G::RPI) + 1];
-    update_row<G::VEC / 2>(c, F.s[i], u2, F.s[i]);
+    const float4 c = coef[row0 + i * G::RPI];
+    update_row<G::VEC / 2>(c.z, c.w, F.s[i], u2, F.s[i]);
   }
 }
 
@@ -205,7 +204,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_t1_kernel(c
   using G = Strip<StateT, CW>;
   constexpr int SPLIT = kD / (CW * NW);
   static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
-  __shared__ float4 s_coef[NW][kCoefPerRow * kD];
+  __shared__ float4 s_coef[NW][kD];
 
   const int split = blockIdx.x % SPLIT;
   const int unit = blockIdx.x / SPLIT;
@@ -270,7 +269,7 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
   static_assert(CW * NW == kD, "one CTA covers all value columns");
   __shared__ float s_a[3 * kD];  // SiLU(conv) of this head's q | k | v channels
   __shared__ float s_d[kD];      // decay exp(g)
-  __shared__ float4 s_coef[NW][kCoefPerRow * kD];
+  __shared__ float4 s_coef[NW][kD];
   __shared__ float s_ss[NW];
 
   const int unit = blockIdx.x;
@@ -383,7 +382,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
   constexpr int SPLIT = kD / (CW * NW);
   constexpr int TC = 8;
   static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
-  __shared__ float4 s_coef[TC][kCoefPerRow * kD];
+  __shared__ float4 s_coef[TC][kD];
   __shared__ float2 s_tok[TC];  // (beta, q.k)
 
   const int split = blockIdx.x % SPLIT;

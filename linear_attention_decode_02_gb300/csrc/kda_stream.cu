@@ -12,8 +12,8 @@
 //                  coefficient array (d k, d q, d, k) and q.k; then `ready`.
 //   8 consumers    per unit: a 16-column strip over all 128 key rows from
 //                  shared memory: the two k-reductions (in-thread plus xor
-//                  shuffles), u and o, the update written straight from
-//                  registers to global, release of the stage (`empty`); (fused:
+//                  shuffles), u and o, release of the stage (`empty`), the
+//                  update written straight from registers to global; (fused:
 //                  the gated RMSNorm through one named barrier per unit).
 //
 // Three (float32) or five (bfloat16) stages keep ~200 KB of state loads in
@@ -31,11 +31,11 @@ __device__ unsigned int g_kda_device_error = 0;
 __device__ __forceinline__ void record_error(unsigned int bit) { atomicOr(&g_kda_device_error, bit); }
 
 // Consumer core shared by the stream kernels: reads the lane's fragments of
-// a swizzled stage into registers and accumulates the column-pair sums of
-// the two k-reductions.
+// a swizzled stage into registers, keeps each row's (decay, key) pair, and
+// accumulates the column-pair sums of the two k-reductions.
 template <typename StateT, typename G>
 __device__ __forceinline__ void reduce_stage(const unsigned char* st, const float4* coef, int row0, int col0,
-                                             typename Frag<StateT>::Raw (&S)[G::PASSES],
+                                             typename Frag<StateT>::Raw (&S)[G::PASSES], float2 (&dk)[G::PASSES],
                                              float2 (&acc_a)[G::VEC / 2], float2 (&acc_b)[G::VEC / 2]) {
 #pragma unroll
   for (int p = 0; p < G::VEC / 2; ++p) { acc_a[p] = make_float2(0.f, 0.f); acc_b[p] = make_float2(0.f, 0.f); }
@@ -43,28 +43,29 @@ __device__ __forceinline__ void reduce_stage(const unsigned char* st, const floa
   for (int i = 0; i < G::PASSES; ++i) {
     const int r = row0 + i * G::RPI;
     S[i] = *reinterpret_cast<const typename Frag<StateT>::Raw*>(st + swz_offset<StateT>(r, col0));
+    const float4 c = coef[r];
+    dk[i] = make_float2(c.z, c.w);
     float2 x2[G::VEC / 2];
 #pragma unroll
     for (int p = 0; p < G::VEC / 2; ++p) x2[p] = Frag<StateT>::get2(S[i], p);
-    accumulate_row<G::VEC / 2>(coef[kCoefPerRow * r], x2, acc_a, acc_b);
+    accumulate_row<G::VEC / 2>(c, x2, acc_a, acc_b);
   }
 }
 
 // S' = d S + k u^T from the registers of reduce_stage, stored to global.
 template <typename StateT, typename G>
-__device__ __forceinline__ void update_store_regs(StateT* sp, const float4* coef, int row0, int col0,
+__device__ __forceinline__ void update_store_regs(StateT* sp, int row0, int col0,
                                                   const typename Frag<StateT>::Raw (&S)[G::PASSES],
-                                                  const float (&u)[G::VEC]) {
+                                                  const float2 (&dk)[G::PASSES], const float (&u)[G::VEC]) {
   float2 u2[G::VEC / 2];
   pairs_of<G::VEC>(u, u2);
 #pragma unroll
   for (int i = 0; i < G::PASSES; ++i) {
-    const int r = row0 + i * G::RPI;
     float2 x2[G::VEC / 2], y2[G::VEC / 2];
 #pragma unroll
     for (int p = 0; p < G::VEC / 2; ++p) x2[p] = Frag<StateT>::get2(S[i], p);
-    update_row<G::VEC / 2>(coef[kCoefPerRow * r + 1], x2, u2, y2);
-    Frag<StateT>::store(sp + r * kD + col0, Frag<StateT>::pack2(y2));
+    update_row<G::VEC / 2>(dk[i].x, dk[i].y, x2, u2, y2);
+    Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(y2));
   }
 }
 
@@ -195,7 +196,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
         d.y = expf(log_decay(gr.y + dtb.y, A, a.gate_mode, a.lower_bound));
         d.z = expf(log_decay(gr.z + dtb.z, A, a.gate_mode, a.lower_bound));
         d.w = expf(log_decay(gr.w + dtb.w, A, a.gate_mode, a.lower_bound));
-        const float qk = token_coefficients(q, k, d, lane, coef_all + s * C::COEF_PER_STAGE);
+        const float qk = token_coefficients(q, k, d, lane, coef_all + s * kD);
         if (lane == 0) scal[s].w = __float_as_int(qk);
       }
       __syncwarp();
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       continue;
     }
     const unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
-    const float4* coef = coef_all + s * C::COEF_PER_STAGE;
+    const float4* coef = coef_all + s * kD;
     float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
     float vv[G::VEC];
 #pragma unroll
@@ -234,8 +235,12 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       const float4 t = lds4(st + C::STATE_BYTES + 2 * T1_ACT_SLOT, col0 + jj, a.qkv_dtype);
       vv[jj] = t.x; vv[jj + 1] = t.y; vv[jj + 2] = t.z; vv[jj + 3] = t.w;
     }
+    // k-reductions; the decay and key coefficients of each row stay in registers
     typename Frag<StateT>::Raw S[G::PASSES];
-    reduce_stage<StateT, G>(st, coef, row0, col0, S, acc2_a, acc2_b);
+    float2 dk[G::PASSES];
+    reduce_stage<StateT, G>(st, coef, row0, col0, S, dk, acc2_a, acc2_b);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the stage
     float acc_a[G::VEC], acc_b[G::VEC];
     strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
     const float beta = __int_as_float(sc.y);
@@ -247,9 +252,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       o[jj] = a.scale * (acc_b[jj] + qk * u_[jj]);
     }
     StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
-    update_store_regs<StateT, G>(sp, coef, row0, col0, S, u_);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the stage or its coefficients
+    update_store_regs<StateT, G>(sp, row0, col0, S, dk, u_);
     if (row0 == 0) store_out<G::VEC>(out + col0, o);
   }
 }
@@ -420,7 +423,7 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         d.w = expf(log_decay(gr.w + dtb.w, A, a.gate_mode, a.lower_bound));
         const float4 q = reinterpret_cast<const float4*>(conv)[lane];
         const float4 k = reinterpret_cast<const float4*>(conv + kD)[lane];
-        const float qk = token_coefficients(q, k, d, lane, coef_all + s * C::COEF_PER_STAGE);
+        const float qk = token_coefficients(q, k, d, lane, coef_all + s * kD);
         if (lane == 0) scal[s].w = __float_as_int(qk);
       }
       __syncwarp();
@@ -448,7 +451,7 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
     float ss = 0.f;
     if (live) {
       const unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
-      const float4* coef = coef_all + s * C::COEF_PER_STAGE;
+      const float4* coef = coef_all + s * kD;
       const float* conv = conv_all + s * 3 * kD;
       float vv[G::VEC];
 #pragma unroll
@@ -459,8 +462,11 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         og[jj] = t.x; og[jj + 1] = t.y; og[jj + 2] = t.z; og[jj + 3] = t.w;
       }
       typename Frag<StateT>::Raw S[G::PASSES];
+      float2 dk[G::PASSES];
       float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
-      reduce_stage<StateT, G>(st, coef, row0, col0, S, acc2_a, acc2_b);
+      reduce_stage<StateT, G>(st, coef, row0, col0, S, dk, acc2_a, acc2_b);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
       float acc_a[G::VEC], acc_b[G::VEC];
       strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
       const float beta = __int_as_float(sc.y);
@@ -473,9 +479,7 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         ss = fmaf(o[jj], o[jj], ss);
       }
       StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
-      update_store_regs<StateT, G>(sp, coef, row0, col0, S, u_);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);  // stage and coefficients no longer read
+      update_store_regs<StateT, G>(sp, row0, col0, S, dk, u_);
     } else if (ok) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);

@@ -22,7 +22,7 @@ struct SwzCfg {
 };
 
 // Ring of NSTAGE stages: [state block | ACT_BYTES of unit vectors] each
-// (1024-byte aligned), then per stage a coefficient array (2 float4 per key row),
+// (1024-byte aligned), then per stage a coefficient array (128 float4),
 // DERIVED_BYTES of prologue results, scalars (int4) and three mbarriers.
 template <typename StateT, uint32_t ACT_BYTES, int NSTAGE_, uint32_t DERIVED_BYTES = 0>
 struct StageCfg : SwzCfg<StateT> {
@@ -31,8 +31,7 @@ struct StageCfg : SwzCfg<StateT> {
   static constexpr int CW = 16;  // columns per consumer warp
   static constexpr uint32_t STAGE_BYTES = ((SwzCfg<StateT>::STATE_BYTES + ACT_BYTES + 1023) / 1024) * 1024;
   static constexpr size_t COEF_OFF = (size_t)NSTAGE * STAGE_BYTES;
-  static constexpr size_t COEF_PER_STAGE = (size_t)kCoefPerRow * kD;  // float4 entries
-  static constexpr size_t DERIVED_OFF = COEF_OFF + (size_t)NSTAGE * COEF_PER_STAGE * sizeof(float4);
+  static constexpr size_t DERIVED_OFF = COEF_OFF + (size_t)NSTAGE * kD * sizeof(float4);
   static constexpr size_t SCAL_OFF = DERIVED_OFF + (size_t)NSTAGE * DERIVED_BYTES;
   static constexpr size_t BAR_OFF = SCAL_OFF + (size_t)NSTAGE * sizeof(int4);
   static constexpr size_t TAIL_OFF = BAR_OFF + 3 * NSTAGE * sizeof(uint64_t);  // kernel-specific extras
