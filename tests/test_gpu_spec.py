@@ -86,6 +86,18 @@ def test_spec_long_rows_span_several_token_chunks():
     _check(case, d, before, out)
 
 
+def test_spec_strong_decay_splits_chunks():
+    """Log decays near the clamp force one-token chunks; results stay at parity."""
+    case = synth.spec_case(3, 6, seed=9, H=2, lengths=[6, 3, 5])
+    gen = torch.Generator().manual_seed(3)
+    case["g"] = -(40.0 + 15.0 * torch.rand(case["g"].shape, generator=gen))
+    d = P.to_device(case)
+    before = d["state"].clone()
+    out = _run(d, 6)
+    torch.cuda.synchronize()
+    _check(case, d, before, out)
+
+
 def test_spec_precomputed_beta():
     case = synth.spec_case(6, 3, seed=4, H=3)
     case["beta"] = torch.rand(case["beta"].shape, generator=torch.Generator().manual_seed(1))
@@ -98,10 +110,9 @@ def test_spec_precomputed_beta():
 
 @pytest.mark.parametrize("split", [8, 0])
 def test_spec_equals_sequential_single_token_calls(split):
-    """One T-token call == T calls of one token per row: bitwise for fp32 state
-    under one kernel configuration (split 8 here), within the fp32 state and
-    output tolerances under the policy, which may pick another split for the
-    smaller single-token calls (a different shuffle-reduction order)."""
+    """One T-token call == T calls of one token per row, within the fp32 state
+    and output tolerances (the T-token call defers the decay within a token
+    chunk, a different rounding order from T single-token calls)."""
     binding.kda_set_split_override(split)
     case = synth.spec_case(12, 6, seed=5, H=16)
     lens, cu = case["lengths"], case["cu_seqlens"]
@@ -120,12 +131,8 @@ def test_spec_equals_sequential_single_token_calls(split):
         out_seq[tok.cuda()] = o
     torch.cuda.synchronize()
     binding.kda_set_split_override(0)
-    if split:
-        assert torch.equal(d["state"], d2["state"])
-        assert torch.equal(out_all, out_seq)
-    else:
-        assert (d["state"] - d2["state"]).abs().max().item() <= P.F32_STATE_ATOL
-        assert (out_all.float() - out_seq.float()).abs().max().item() <= P.OUT_ATOL
+    assert (d["state"] - d2["state"]).abs().max().item() <= P.F32_STATE_ATOL
+    assert (out_all.float() - out_seq.float()).abs().max().item() <= P.OUT_ATOL
 
 
 def test_spec_trailing_empty_rows_golden():
