@@ -397,6 +397,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
   __shared__ float4 s_coef[TC][kD];  // staged (q, k, g), then (P k, P q, k / P, k / P)
   __shared__ float4 s_tok[TC];       // (beta, q.k, largest per-row decay, -)
   __shared__ float s_P[kD];          // P at the chunk end, per key row
+  __shared__ __align__(16) float s_v[TC][kD];  // the chunk's value vectors
 
   const int split = blockIdx.x % SPLIT;
   const int unit = blockIdx.x / SPLIT;
@@ -438,6 +439,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
       const int t = tc0 + j;
       const float4 q = load4(a.q, (int64_t)t * a.q_rs + (int64_t)h * a.q_hs + 4 * lane, a.qkv_dtype);
       const float4 k = load4(a.k, (int64_t)t * a.k_rs + (int64_t)h * a.k_hs + 4 * lane, a.qkv_dtype);
+      reinterpret_cast<float4*>(s_v[j])[lane] =
+          load4(a.v, (int64_t)t * a.v_rs + (int64_t)h * a.v_hs + 4 * lane, a.qkv_dtype);
       float4 g = __ldg(reinterpret_cast<const float4*>(a.g + (int64_t)t * a.g_rs + (int64_t)h * a.g_hs + 4 * lane));
       g = make_float4(fmaxf(g.x, kSpecLogDecayFloor), fmaxf(g.y, kSpecLogDecayFloor),
                       fmaxf(g.z, kSpecLogDecayFloor), fmaxf(g.w, kSpecLogDecayFloor));
@@ -486,7 +489,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
     for (int j = 0; j < ne; ++j) {
       const int t = tc0 + j;
       float vv[G::VEC];
-      load_cols<G::VEC>(a.v, (int64_t)t * a.v_rs + (int64_t)h * a.v_hs + col0, a.qkv_dtype, vv);
+#pragma unroll
+      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = s_v[j][col0 + jj];
       const float4 tk = s_tok[j];
       float acc_a[G::VEC], acc_b[G::VEC];
       strip_reduce<G>(S, s_coef[j], row0, acc_a, acc_b);

@@ -7,7 +7,8 @@
 //                  unit's activation vectors, all completing on the stage's
 //                  `full` barrier.
 //   prologue warps per unit, once, units dealt round-robin: (fused: the short conv + SiLU of the
-//                  head's 384 channels and the conv-cache shift) the L2 norms,
+//                  head's 384 channels, and the conv-cache shift written back
+//                  from the stage with bulk stores) the L2 norms,
 //                  gate and decay of the 128 key channels into the stage's
 //                  coefficient array (d k, d q, d, k) and q.k; then `ready`.
 //   8 consumers    per unit: a 16-column strip over all 128 key rows from
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&ready[s], 1);
-      mbar_init(&empty[s], C::NW);
+      mbar_init(&empty[s], C::NW + 1);  // consumers + the prologue warp (its cache write-back reads the stage)
     }
     mbar_fence_init();
   }
@@ -392,25 +393,35 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(act + F_X);
         const __nv_bfloat16* css = reinterpret_cast<const __nv_bfloat16*>(act + F_CS);
         float* conv = conv_all + s * 3 * kD;
-        __nv_bfloat16* csg = static_cast<__nv_bfloat16*>(a.conv_state) + (int64_t)sc.x * a.cs_slot_stride + h * kD;
-#pragma unroll 4
+        if (lane == 0) {
+          // The shifted cache [tap1, tap2, x] is already in the stage: nine bulk stores.
+          fence_proxy_async_smem();
+          __nv_bfloat16* csg = static_cast<__nv_bfloat16*>(a.conv_state) + (int64_t)sc.x * a.cs_slot_stride + h * kD;
+#pragma unroll
+          for (int sec = 0; sec < 3; ++sec) {
+            bulk_store(csg + sec * HD, act + F_CS + (1 * 3 + sec) * 256, 256);
+            bulk_store(csg + a.cs_tap_stride + sec * HD, act + F_CS + (2 * 3 + sec) * 256, 256);
+            bulk_store(csg + 2 * a.cs_tap_stride + sec * HD, act + F_X + sec * 256, 256);
+          }
+          bulk_commit();
+        }
+        float wv[12][4];  // all the head's conv weights in flight at once
+#pragma unroll
+        for (int i = 0; i < 12; ++i) {
+          const int sec = i >> 2, c = (lane + 32 * i) & (kD - 1);
+          const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + c;
+#pragma unroll
+          for (int tap = 0; tap < 4; ++tap) wv[i][tap] = __ldg(w + tap * HD);
+        }
+#pragma unroll
         for (int i = 0; i < 12; ++i) {  // channel lc = lane + 32 i of the head's 384
           const int lc = lane + 32 * i;
           const int sec = i >> 2, c = lc & (kD - 1);
-          const __nv_bfloat16 xb = xs[lc];
-          const __nv_bfloat16 c0 = css[(0 * 3 + sec) * kD + c];
-          const __nv_bfloat16 c1 = css[(1 * 3 + sec) * kD + c];
-          const __nv_bfloat16 c2 = css[(2 * 3 + sec) * kD + c];
-          const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + c;
-          float y = __ldg(w) * __bfloat162float(c0);
-          y = fmaf(__ldg(w + HD), __bfloat162float(c1), y);
-          y = fmaf(__ldg(w + 2 * HD), __bfloat162float(c2), y);
-          y = fmaf(__ldg(w + 3 * HD), __bfloat162float(xb), y);
+          float y = wv[i][0] * __bfloat162float(css[(0 * 3 + sec) * kD + c]);
+          y = fmaf(wv[i][1], __bfloat162float(css[(1 * 3 + sec) * kD + c]), y);
+          y = fmaf(wv[i][2], __bfloat162float(css[(2 * 3 + sec) * kD + c]), y);
+          y = fmaf(wv[i][3], __bfloat162float(xs[lc]), y);
           conv[lc] = y * sigmoidf_(y);
-          __nv_bfloat16* cp = csg + sec * HD + c;  // cache <- [c1, c2, x]
-          cp[0] = c1;
-          cp[a.cs_tap_stride] = c2;
-          cp[2 * a.cs_tap_stride] = xb;
         }
         __syncwarp();
         const float A = __int_as_float(sc.z);
@@ -427,8 +438,13 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         if (lane == 0) scal[s].w = __float_as_int(qk);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ready[s]);
+      if (lane == 0) {
+        mbar_arrive(&ready[s]);
+        bulk_wait_read();  // the cache write-back no longer reads the stage
+        mbar_arrive(&empty[s]);
+      }
     }
+    if (lane == 0) bulk_wait_all();
     return;
   }
 
