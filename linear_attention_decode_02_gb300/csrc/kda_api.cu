@@ -262,7 +262,8 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
 //    ~95% of copy bandwidth at B >= 128 and beats the streaming kernel;
 //  - bfloat16 state, T=1: the streaming kernel once the units fill five per
 //    SM (packed K3 B >= 64), the split kernel below;
-//  - fused: the streaming kernel from sixteen units per SM, split below;
+//  - fused: the streaming kernel from five units per SM (H=32 rows=256
+//    fp32: 88 % vs 68 % split; rows=32: 59 % vs 52 %), split below;
 //  - speculative rows: the split kernel.
 int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)t_max;
@@ -270,7 +271,7 @@ int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   const int forced = g_schedule_override.load();
   if (forced != KDA_SCHED_AUTO) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
-  if (op == KDA_OP_FUSED) return units >= 16LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
+  if (op == KDA_OP_FUSED) return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
   if (state_dtype == KDA_F32) return KDA_SCHED_SPLIT;
   return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
 }

@@ -268,7 +268,8 @@ def test_schedule_override_and_plan(lib):
     assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == 1  # fp32: split kernel
     assert binding.kda_plan_schedule(0, 16384, 1, 1, 152) == 2  # bf16 state: stream
     assert binding.kda_plan_schedule(2, 8192, 0, 1, 152) == 2  # fused, many units
-    assert binding.kda_plan_schedule(2, 1024, 0, 1, 152) == 1
+    assert binding.kda_plan_schedule(2, 1024, 0, 1, 152) == 2
+    assert binding.kda_plan_schedule(2, 256, 0, 1, 152) == 1
     assert lib.kda_set_split_override(8) == OK  # a forced split implies the split schedule
     assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 1
     assert lib.kda_set_split_override(0) == OK
