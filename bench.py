@@ -106,14 +106,6 @@ class Workload:
     def step(self, i):
         self.call(self.sets[i % len(self.sets)])
 
-    def e2e_step(self, i, host, dev_idx):
-        for k, t in host.items():
-            if k != "idx":
-                self.d[k].copy_(t, non_blocking=True)
-        dev_idx.copy_(host["idx"][i % len(host["idx"])], non_blocking=True)
-        self.call(dev_idx)
-        self.out_h.copy_(self.out, non_blocking=True)
-
 
 class Recurrent(Workload):
     def __init__(self, B=512, H=32, slots=1024, state_dtype=torch.float32, n_sets=2, null_count=0, seed=0,
@@ -384,15 +376,66 @@ def time_graph(wl, n_calls, reps, flush):
 
 
 def e2e(wl, steps, warmup, barrier):
-    """The same call with pinned-host activations and indices copied in, the output copied out."""
-    host = {k: wl.d[k].cpu().pin_memory() for k in wl.e2e_keys}
-    host["idx"] = [s.cpu().pin_memory() for s in wl.sets]
-    wl.out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
-    dev_idx = torch.empty_like(wl.sets[0])
-    ms, _ = time_direct(lambda i: wl.e2e_step(i, host, dev_idx), steps, warmup, barrier)
-    h2d = sum(host[k].numel() * host[k].element_size() for k in wl.e2e_keys) + host["idx"][0].numel() * 4
-    d2h = wl.out_h.numel() * wl.out_h.element_size()
-    return ms, h2d, d2h
+    """The same call end to end: every step copies its activations and slot
+    indices from pinned host memory to the device and its output back.
+
+    The steps are pipelined the way a serving loop would run them: inputs
+    and outputs are double-buffered on the device, host-to-device copies run
+    on one side stream and device-to-host copies on another, and events keep
+    step i's copies ordered with its kernel; the state pool is updated in
+    place on the compute stream, so kernels stay in order.
+    """
+    keys = wl.e2e_keys
+    nb = 2
+    host = [{k: wl.d[k].cpu().pin_memory() for k in keys} for _ in range(nb)]
+    host_idx = [s.cpu().pin_memory() for s in wl.sets]
+    dev = [{k: wl.d[k].clone() for k in keys} for _ in range(nb)]
+    dev_idx = [torch.empty_like(wl.sets[0]) for _ in range(nb)]
+    outs = [torch.empty_like(wl.out) for _ in range(nb)]
+    out_h = [torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory() for _ in range(nb)]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(nb)]
+    ev_k = [torch.cuda.Event() for _ in range(nb)]
+    ev_out = [torch.cuda.Event() for _ in range(nb)]
+    base = dict(wl.d)
+
+    def step(i):
+        b = i % nb
+        s_in.wait_event(ev_k[b])  # the kernel two steps back has read this input buffer
+        with torch.cuda.stream(s_in):
+            for k in keys:
+                dev[b][k].copy_(host[b][k], non_blocking=True)
+            dev_idx[b].copy_(host_idx[i % len(host_idx)], non_blocking=True)
+        ev_in[b].record(s_in)
+        comp.wait_event(ev_in[b])
+        comp.wait_event(ev_out[b])  # the output buffer has been copied out
+        wl.d = {**base, **dev[b]}
+        wl.out = outs[b]
+        wl.call(dev_idx[b])
+        ev_k[b].record(comp)
+        s_out.wait_event(ev_k[b])
+        with torch.cuda.stream(s_out):
+            out_h[b].copy_(outs[b], non_blocking=True)
+        ev_out[b].record(s_out)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    for i in range(warmup, warmup + steps):
+        step(i)
+    for b in range(nb):
+        comp.wait_event(ev_out[b])  # the timed region ends with the last outputs on the host
+    e1.record(comp)
+    torch.cuda.synchronize()
+    barrier()
+    wl.d = base
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in keys) + host_idx[0].numel() * 4
+    d2h = out_h[0].numel() * out_h[0].element_size()
+    return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
 def path_measurements(flush, peak):

@@ -230,11 +230,19 @@ kda_status kda_set_schedule_override(int32_t schedule);
 /*
  * Device error word of the streaming kernels on the current device: bit 0 =
  * a wait for a filled stage timed out (2 s), bit 1 = a wait for a free stage
- * timed out.  A kernel that times out records the bit and returns early, its
+ * timed out, bit 2 = the kda_selftest_wait_timeout wait gave up (expected).  A kernel that times out records the bit and returns early, its
  * results for the affected units are undefined.  Synchronises the device;
  * clears the word when `clear` is non-zero.
  */
 kda_status kda_device_error(uint32_t* flags, int32_t clear);
+
+/*
+ * Diagnostic of the bounded waits: launches one warp on `stream` that waits
+ * on a barrier nothing completes.  The wait gives up after 2 s and sets bit
+ * 2 (value 4) of the device error word, so the timeout path can be checked
+ * without faulting or hanging the GPU; the context stays usable.
+ */
+kda_status kda_selftest_wait_timeout(void* stream);
 
 const char* kda_status_string(kda_status s);
 /* Detail of the last non-OK status returned on the calling thread. */

@@ -31,7 +31,8 @@ DEFAULT_SCALE = 1.0 / math.sqrt(128.0)
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_recurrent_decode", "kda_packed_decode", "kda_fused_decode", "kda_spec_decode",
            "kda_plan_split", "kda_set_split_override", "kda_plan_schedule", "kda_set_schedule_override",
-           "kda_device_error", "kda_status_string", "kda_last_error_message", "kda_version")
+           "kda_device_error", "kda_selftest_wait_timeout", "kda_status_string", "kda_last_error_message",
+           "kda_version")
 SCHED_AUTO, SCHED_SPLIT, SCHED_STREAM = 0, 1, 2
 
 
@@ -71,6 +72,8 @@ def _declare(lib):
     lib.kda_set_schedule_override.restype = ctypes.c_int
     lib.kda_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     lib.kda_device_error.restype = ctypes.c_int
+    lib.kda_selftest_wait_timeout.argtypes = [vp]
+    lib.kda_selftest_wait_timeout.restype = ctypes.c_int
     lib.kda_status_string.argtypes = [ctypes.c_int]
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_last_error_message.argtypes = []
@@ -211,6 +214,15 @@ def kda_device_error(clear=True):
     flags = ctypes.c_uint32(0)
     _check(lib, lib.kda_device_error(ctypes.byref(flags), int(bool(clear))))
     return int(flags.value)
+
+
+def kda_selftest_wait_timeout(device=None):
+    """Launch the bounded-wait self-test on the current stream (sets device error bit 2 after ~2 s)."""
+    lib = library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        st = lib.kda_selftest_wait_timeout(ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream))
+    _check(lib, st)
 
 
 def kda_version():

@@ -675,6 +675,13 @@ kda_status kda_device_error(uint32_t* flags, int32_t clear) {
   return KDA_OK;
 }
 
+kda_status kda_selftest_wait_timeout(void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  KDA_TRY(current_device(st, &dev));
+  return check_launch(kda::launch_selftest_wait(st));
+}
+
 kda_status kda_set_split_override(int32_t split) {
   KDA_CHECK(split == 0 || kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
   g_split_override.store(split);

@@ -76,6 +76,9 @@ cudaError_t launch_t1_stream(const T1Args& a, int state_dtype, int sm_count, cud
 // slots, raw-gate and output-gate head vectors.
 cudaError_t launch_fused_stream(const FusedArgs& a, int state_dtype, int sm_count, cudaStream_t s);
 
+// One warp waiting on a barrier nothing completes (bounded-wait self-test).
+cudaError_t launch_selftest_wait(cudaStream_t s);
+
 // Reads (and optionally clears) the device error word of the streaming
 // kernels: bit 0 = a stage-full wait timed out, bit 1 = a stage-free wait.
 cudaError_t read_device_error(unsigned int* flags, bool clear);

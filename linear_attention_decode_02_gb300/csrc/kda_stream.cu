@@ -26,7 +26,8 @@
 
 namespace kda {
 
-// bit 0: a stage-full/ready wait timed out; bit 1: a stage-free wait timed out.
+// bit 0: a stage-full/ready wait timed out; bit 1: a stage-free wait timed
+// out; bit 2: the self-test wait timed out (expected).
 __device__ unsigned int g_kda_device_error = 0;
 
 __device__ __forceinline__ void record_error(unsigned int bit) { atomicOr(&g_kda_device_error, bit); }
@@ -524,6 +525,19 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
   }
 }
 
+// Self-test of the bounded wait: one warp waits on a barrier that nothing
+// completes; the wait gives up after kWaitNs and records bit 2.
+__global__ void kda_selftest_wait_kernel() {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait(&bar, 0);
+  if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) record_error(4u);
+}
+
 // ---- host side ------------------------------------------------------------------------
 
 namespace {
@@ -580,6 +594,11 @@ cudaError_t launch_t1_stream(const T1Args& a, int state_dtype, int sm_count, cud
 cudaError_t launch_fused_stream(const FusedArgs& a, int state_dtype, int sm_count, cudaStream_t s) {
   if (state_dtype == KDA_DT_F32) return launch_fused_stream_typed<float>(a, sm_count, s);
   return launch_fused_stream_typed<__nv_bfloat16>(a, sm_count, s);
+}
+
+cudaError_t launch_selftest_wait(cudaStream_t s) {
+  kda_selftest_wait_kernel<<<1, 32, 0, s>>>();
+  return cudaGetLastError();
 }
 
 cudaError_t read_device_error(unsigned int* flags, bool clear) {
