@@ -374,57 +374,30 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
 // =====================================================================================
 // Speculative T >= 1: one CTA per (row, head, split); the state stays in
 // float32 registers across the row's tokens.  Tokens are staged TC at a
-// time (a chunk) and processed TS at a time (a sub-chunk).
-//
-// Deferred decay.  With P_t the cumulative decay of each key row since the
-// chunk start, the registers hold S~ = S / P_t.  Token t then reads the
-// state through c_a = P_t k and c_b = P_t q and writes it through
-// c_u = k / P_t (S~ += c_u u_t^T); the true state P_end S~ is restored at
-// chunk end.  A chunk ends early once the sum over its tokens of the
-// largest per-row decay exceeds e^-80, keeping P_t and 1/P_t finite in
-// float32 (per-element log decays are clamped at -60: anything decayed
-// further is below float32 resolution of the rest of the row).
-//
-// Sub-chunk form.  All TS tokens of a sub-chunk read the sub-chunk-start
-// state S~ in one pass (a'_t = c_a(t)^T S~, b'_t = c_b(t)^T S~), then per
-// value column
-//     u_t = beta_t (v_t - a'_t - sum_{tau<t} alpha(t,tau) u_tau)
-//     o_t = scale (b'_t + (q.k)_t u_t + sum_{tau<t} gamma(t,tau) u_tau)
-// with alpha(t,tau) = c_a(t).c_u(tau) and gamma(t,tau) = c_b(t).c_u(tau)
-// (tau in the same sub-chunk), and one pass applies S~ += sum_t c_u(t) u_t^T.
-// This is the sequential recurrence regrouped: the same products, with one
-// shuffle reduction and one dependency chain per sub-chunk instead of per
-// token.
+// time.  Within a chunk the decay is deferred: with P_t the cumulative decay
+// of each key row since the chunk start, the registers hold S~ = S / P_t, so
+// the reductions use (P_t k, P_t q) and the update is one paired FMA,
+// S~ += (k / P_t) u^T; the true state P_end S~ is restored at chunk end.  A
+// chunk ends early once the sum over its tokens of the largest per-row decay
+// exceeds e^-80, keeping P_t and 1/P_t finite in float32 (per-element log
+// decays are clamped at -60: anything decayed further is below float32
+// resolution of the rest of the row).
 // Grid slice n == N zeroes the padding token rows outside [cu[0], cu[N]).
 // =====================================================================================
 constexpr float kSpecMaxLogDecay = 80.f;   // chunk bound on the summed per-token decay
 constexpr float kSpecLogDecayFloor = -60.f;
-constexpr int kSpecTC = 8;                 // tokens staged per chunk
-
-// Tokens per sub-chunk: the accumulators of all its tokens live in registers
-// next to the state (4 for float32 state: 4 columns per lane; 2 for bf16:
-// 8 columns per lane).
-template <typename StateT>
-struct SpecSub {
-  static constexpr int TS = sizeof(StateT) == 4 ? 4 : 2;
-};
 
 template <typename StateT, int CW, int NW>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel(const SpecArgs a) {
   using G = Strip<StateT, CW>;
-  constexpr int NP = G::VEC / 2;  // column pairs per lane
   constexpr int SPLIT = kD / (CW * NW);
-  constexpr int TC = kSpecTC;
-  constexpr int TS = SpecSub<StateT>::TS;
+  constexpr int TC = 8;
   constexpr int NT = NW * 32;
   static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
-  static_assert(TC % TS == 0, "sub-chunks tile a chunk");
-  __shared__ float4 s_coef[TC][kD];  // staged (q, k, g, -), then (P k, P q, k / P, k / P)
+  __shared__ float4 s_coef[TC][kD];  // staged (q, k, g), then (P k, P q, k / P, k / P)
   __shared__ float4 s_tok[TC];       // (beta, q.k, largest per-row decay, -)
   __shared__ float s_P[kD];          // P at the chunk end, per key row
   __shared__ __align__(16) float s_v[TC][kD];  // the chunk's value vectors
-  __shared__ float s_al[TC][TS];     // alpha(t, tau), tau indexed within t's sub-chunk
-  __shared__ float s_ga[TC][TS];     // gamma(t, tau)
 
   const int split = blockIdx.x % SPLIT;
   const int unit = blockIdx.x / SPLIT;
@@ -461,7 +434,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
   for (int tc0 = t0; tc0 < t1;) {
     const int nt = min(TC, t1 - tc0);
     if (tc0 != t0) __syncthreads();  // previous chunk fully consumed
-    // per-token prologue, one token per warp: normalised q, k, the log decay and v
+    // per-token prologue, one token per warp: normalised q, k and the log decay
     for (int j = warp; j < nt; j += NW) {
       const int t = tc0 + j;
       const float4 q = load4(a.q, (int64_t)t * a.q_rs + (int64_t)h * a.q_hs + 4 * lane, a.qkv_dtype);
@@ -513,104 +486,38 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
       s_P[r] = P;
     }
     __syncthreads();
-    // alpha / gamma for token pairs inside each sub-chunk, one pair per warp
-    {
-      int p = 0;
-      for (int t = 1; t < ne; ++t) {
-        const int s0 = (t / TS) * TS;
-        for (int tau = s0; tau < t; ++tau, ++p) {
-          if (p % NW != warp) continue;
-          float al = 0.f, ga = 0.f;
+    for (int j = 0; j < ne; ++j) {
+      const int t = tc0 + j;
+      float vv[G::VEC];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float4 ct = s_coef[t][4 * lane + i];
-            const float cu = s_coef[tau][4 * lane + i].z;
-            al = fmaf(ct.x, cu, al);
-            ga = fmaf(ct.y, cu, ga);
-          }
-          al = warp_sum(al);
-          ga = warp_sum(ga);
-          if (lane == 0) {
-            s_al[t][tau - s0] = al;
-            s_ga[t][tau - s0] = ga;
-          }
-        }
+      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = s_v[j][col0 + jj];
+      const float4 tk = s_tok[j];
+      float acc_a[G::VEC], acc_b[G::VEC];
+      strip_reduce<G>(S, s_coef[j], row0, acc_a, acc_b);
+      float u[G::VEC], o[G::VEC];
+#pragma unroll
+      for (int jj = 0; jj < G::VEC; ++jj) {
+        u[jj] = tk.x * (vv[jj] - acc_a[jj]);
+        o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
       }
-    }
-    __syncthreads();
-
-    for (int s0 = 0; s0 < ne; s0 += TS) {
-      const int ns = min(TS, ne - s0);
-      // every token of the sub-chunk reads the sub-chunk-start state
-      float2 A2[TS][NP], B2[TS][NP];
-#pragma unroll
-      for (int t = 0; t < TS; ++t)
-#pragma unroll
-        for (int p = 0; p < NP; ++p) { A2[t][p] = make_float2(0.f, 0.f); B2[t][p] = make_float2(0.f, 0.f); }
+      // S~ += (k / P_t) u^T
+      float2 u2[G::VEC / 2];
+      pairs_of<G::VEC>(u, u2);
 #pragma unroll
       for (int i = 0; i < G::PASSES; ++i) {
-        const int r = row0 + i * G::RPI;
+        const float4 c = s_coef[j][row0 + i * G::RPI];
+        const float2 ku = make_float2(c.z, c.w);
 #pragma unroll
-        for (int t = 0; t < TS; ++t) {
-          if (t < ns) {
-            const float4 c = s_coef[s0 + t][r];
-            const float2 ca = dup2(c.x), cb = dup2(c.y);
-#pragma unroll
-            for (int p = 0; p < NP; ++p) {
-              A2[t][p] = fma2(ca, S.s[i][p], A2[t][p]);
-              B2[t][p] = fma2(cb, S.s[i][p], B2[t][p]);
-            }
-          }
-        }
+        for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = fma2(ku, u2[p], S.s[i][p]);
       }
-      // column sums across the lanes sharing the columns, then the recurrence
-      float u[TS][G::VEC];
-#pragma unroll
-      for (int t = 0; t < TS; ++t) {
-        if (t < ns) {
-          float aa[G::VEC], bb[G::VEC];
-          strip_allreduce<G>(A2[t], B2[t], aa, bb);
-          const float4 tk = s_tok[s0 + t];
-          float o[G::VEC];
-#pragma unroll
-          for (int jj = 0; jj < G::VEC; ++jj) {
-            float x = s_v[s0 + t][col0 + jj] - aa[jj];
-            float y = bb[jj];
-#pragma unroll
-            for (int tau = 0; tau < TS; ++tau) {
-              if (tau < t) {
-                x = fmaf(-s_al[s0 + t][tau], u[tau][jj], x);
-                y = fmaf(s_ga[s0 + t][tau], u[tau][jj], y);
-              }
-            }
-            u[t][jj] = tk.x * x;
-            o[jj] = a.scale * fmaf(tk.y, u[t][jj], y);
-          }
-          if (row0 == 0) store_out<G::VEC>(out + (tc0 + s0 + t) * out_rs, o);
-        }
-      }
-      // S~ += sum_t c_u(t) u_t^T
-#pragma unroll
-      for (int i = 0; i < G::PASSES; ++i) {
-        const int r = row0 + i * G::RPI;
-#pragma unroll
-        for (int t = 0; t < TS; ++t) {
-          if (t < ns) {
-            const float4 c = s_coef[s0 + t][r];
-            const float2 ku = make_float2(c.z, c.w);
-#pragma unroll
-            for (int p = 0; p < NP; ++p)
-              S.s[i][p] = fma2(ku, make_float2(u[t][2 * p], u[t][2 * p + 1]), S.s[i][p]);
-          }
-        }
-      }
+      if (row0 == 0) store_out<G::VEC>(out + t * out_rs, o);
     }
     // restore the true state: S = P_end S~
 #pragma unroll
     for (int i = 0; i < G::PASSES; ++i) {
       const float2 pp = dup2(s_P[row0 + i * G::RPI]);
 #pragma unroll
-      for (int p = 0; p < NP; ++p) S.s[i][p] = mul2(pp, S.s[i][p]);
+      for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = mul2(pp, S.s[i][p]);
     }
     tc0 += ne;
   }
