@@ -128,14 +128,14 @@ def gate(raw_g, dt_bias, A_log, lower_bound):
 
 # --- the recurrent step --------------------------------------------------------------
 
-def kda_step(S, q, k, v, g, beta, scale=SCALE):
-    """One KDA decode step for one (row, head) unit.
+def kda_step_u(S, q, k, v, g, beta, scale=SCALE):
+    """One KDA decode step for one (row, head) unit, with its correction.
 
     S is the [K=128][V=128] state (row = key channel); q, k, v, g are [128]
     vectors with g the per-key-channel log decay; beta is the delta-rule
     learning rate.  Steps, in order: L2-normalise q and k; decay the state by
-    diag(exp(g)); delta write S' = S_d + k (beta (v - S_d^T k))^T; output
-    o = scale * S'^T q.  Returns (S', o).
+    diag(exp(g)); delta write S' = S_d + k u^T with the correction
+    u = beta (v - S_d^T k); output o = scale * S'^T q.  Returns (S', o, u).
     """
     S = np.asarray(S, dtype=np.float64)
     qh = l2_normalize(q)
@@ -144,6 +144,12 @@ def kda_step(S, q, k, v, g, beta, scale=SCALE):
     u = float(beta) * (np.asarray(v, np.float64) - Sd.T @ kh)
     S_new = Sd + np.outer(kh, u)
     o = scale * (S_new.T @ qh)
+    return S_new, o, u
+
+
+def kda_step(S, q, k, v, g, beta, scale=SCALE):
+    """One KDA decode step (see kda_step_u); returns (S', o)."""
+    S_new, o, _ = kda_step_u(S, q, k, v, g, beta, scale)
     return S_new, o
 
 
@@ -312,6 +318,55 @@ def spec_decode(q, k, v, g, beta, cu_seqlens, state_indices, state,
                 S, out[t, h] = kda_step(S, q[t, h], k[t, h], v[t, h], g[t, h], rate[t, h], scale)
             state[s, h] = S
     return out, state
+
+
+def spec_verify(q, k, v, g, beta, cu_seqlens, state_indices, state, t_cap,
+                beta_is_logit=True, scale=SCALE):
+    """Speculative-verify mode: the spec_decode outputs from a read-only state.
+
+    "flashinfer.kda_decode", section "Frozen / speculative-verify mode": the
+    committed state is never written; slot-indexed out-params record, for
+    token position t < t_cap of each live row, the delta-rule correction u_t
+    ([M, H, t_cap, 128]) and the token's raw key followed by its log decay
+    ([M, H, t_cap, 256]), for a later commit of the accepted tokens.
+    Returns (out [R, H, 128], correction, kg); untouched entries are zero.
+    """
+    q = np.asarray(q, np.float64)
+    R, H, _ = q.shape
+    state = np.asarray(state, dtype=np.float64)
+    M = state.shape[0]
+    rate = np.asarray(beta, np.float64)
+    if beta_is_logit:
+        rate = sigmoid(rate)
+    out = np.zeros((R, H, D))
+    corr = np.zeros((M, H, t_cap, D))
+    kg = np.zeros((M, H, t_cap, 2 * D))
+    for n in range(len(state_indices)):
+        s = int(state_indices[n])
+        t0, t1 = int(cu_seqlens[n]), int(cu_seqlens[n + 1])
+        if not _is_live(s, M) or t1 <= t0:
+            continue
+        for h in range(H):
+            S = state[s, h]
+            for t in range(t0, t1):
+                S, out[t, h], u = kda_step_u(S, q[t, h], k[t, h], v[t, h], g[t, h], rate[t, h], scale)
+                if t - t0 < t_cap:
+                    corr[s, h, t - t0] = u
+                    kg[s, h, t - t0, :D] = k[t, h]
+                    kg[s, h, t - t0, D:] = g[t, h]
+    return out, corr, kg
+
+
+def commit_from_cache(S, kg_rows, corr_rows):
+    """State after replaying cached tokens: S <- diag(exp(g)) S + k_hat u^T per token.
+
+    kg_rows: [a, 256] raw key | log decay; corr_rows: [a, 128] corrections.
+    """
+    S = np.array(S, dtype=np.float64, copy=True)
+    for kg_t, u in zip(kg_rows, corr_rows):
+        kh = l2_normalize(kg_t[:D])
+        S = np.exp(kg_t[D:])[:, None] * S + np.outer(kh, u)
+    return S
 
 
 # --- rounding helpers used by the tests ----------------------------------------------

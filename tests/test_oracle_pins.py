@@ -362,3 +362,60 @@ def test_spec_precomputed_beta_flag():
     # expit and the oracle's sigmoid may differ in the last bit of beta
     np.testing.assert_allclose(o1, o2, rtol=1e-12, atol=1e-15)
     np.testing.assert_allclose(s1, s2, rtol=1e-12, atol=1e-15)
+
+
+def test_verify_outputs_match_spec_and_leave_state():
+    case = synth.spec_case(6, 5, seed=11, H=2)
+    c = _np(case)
+    out_s, _ = ko.spec_decode(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu_seqlens"],
+                              c["state_indices"], c["state"])
+    before = c["state"].copy()
+    out_v, corr, kg = ko.spec_verify(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu_seqlens"],
+                                     c["state_indices"], c["state"], t_cap=5)
+    np.testing.assert_array_equal(out_v, out_s)
+    np.testing.assert_array_equal(c["state"], before)
+
+
+def test_commit_from_cached_tokens_rebuilds_the_state():
+    """Replaying (k, g, u) of the first a tokens equals the spec state after a tokens."""
+    case = synth.spec_case(5, 6, seed=12, H=2, lengths=[6, 4, 0, 5, 2])
+    c = _np(case)
+    _, corr, kg = ko.spec_verify(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu_seqlens"],
+                                 c["state_indices"], c["state"], t_cap=6)
+    lens, cu, idx = c["lengths"], c["cu_seqlens"], c["state_indices"]
+    rng = np.random.default_rng(0)
+    for n in range(5):
+        if lens[n] == 0:
+            continue
+        acc = int(rng.integers(0, lens[n] + 1))
+        # spec decode of only the accepted tokens of this row
+        cu1 = np.array([0, acc])
+        tok = list(range(int(cu[n]), int(cu[n]) + acc))
+        _, st = ko.spec_decode(c["q"][tok], c["k"][tok], c["v"][tok], c["g"][tok], c["beta"][tok], cu1,
+                               idx[n:n + 1], c["state"])
+        s = int(idx[n])
+        for h in range(2):
+            rebuilt = ko.commit_from_cache(c["state"][s, h], kg[s, h, :acc], corr[s, h, :acc])
+            np.testing.assert_allclose(rebuilt, st[s, h], rtol=1e-12, atol=1e-14)
+
+
+def test_verify_cache_capacity_and_null_rows():
+    case = synth.spec_case(4, 6, seed=13, H=1, lengths=[6, 3, 2, 4], null_count=1)
+    c = _np(case)
+    _, corr, kg = ko.spec_verify(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu_seqlens"],
+                                 c["state_indices"], c["state"], t_cap=3)
+    idx = c["state_indices"]
+    M = c["state"].shape[0]
+    for n in range(4):
+        s = int(idx[n])
+        if not (0 < s < M):
+            continue
+        L = min(int(c["lengths"][n]), 3)
+        t0 = int(c["cu_seqlens"][n])
+        for t in range(L):
+            np.testing.assert_array_equal(kg[s, 0, t, :128], c["k"][t0 + t, 0])
+            np.testing.assert_array_equal(kg[s, 0, t, 128:], c["g"][t0 + t, 0])
+    live = {int(s) for s in idx if 0 < int(s) < M}
+    for s in range(M):
+        if s not in live:
+            assert not corr[s].any() and not kg[s].any()
