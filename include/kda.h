@@ -181,6 +181,30 @@ kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_t
                            const kda_tensor* state_indices, const kda_tensor* state,
                            const kda_tensor* out, float scale, void* stream);
 
+/*
+ * kda_spec_verify_decode — speculative-verify mode ([P1] "Frozen /
+ * speculative-verify mode"): the kda_spec_decode outputs for up to 16 tokens
+ * per row computed from a read-only committed state pool; the state is never
+ * written.  Arguments as kda_spec_decode (state is read only, t_max <= 16),
+ * plus two optional slot-indexed out-params for a later commit of the
+ * accepted tokens (either may be NULL):
+ *   correction_cache [num_slots, H, T_cap, 128] float32 contiguous: for the
+ *                token at position t < T_cap of a live row, its delta-rule
+ *                correction u_t = beta (v - S_d^T k_hat);
+ *   kg_cache     [num_slots, H, T_cap, 256] float32 contiguous: that token's
+ *                raw key (128) followed by its log decay g (128).
+ * T_cap (1..16) is the caches' third extent (equal when both are given).  The
+ * state after accepting the first a tokens of a row is, token by token,
+ * S <- diag(exp(g)) S + normalise(k) u^T.  Null and empty rows write no cache
+ * entry; tokens at positions >= T_cap are decoded but not cached.
+ */
+kda_status kda_spec_verify_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                  const kda_tensor* g, const kda_tensor* beta, int32_t beta_is_logit,
+                                  const kda_tensor* cu_seqlens, int32_t t_max,
+                                  const kda_tensor* state_indices, const kda_tensor* state,
+                                  const kda_tensor* out, const kda_tensor* correction_cache,
+                                  const kda_tensor* kg_cache, float scale, void* stream);
+
 /* ---- host-only queries (no CUDA calls) ---------------------------------- */
 
 /* Operation ids for kda_plan_split. */

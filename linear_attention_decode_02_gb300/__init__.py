@@ -6,6 +6,7 @@ The four decode entry points of libkda, with the C names:
     kda_packed_decode      Kimi K3 packed QKV, T=1, bf16 state
     kda_fused_decode       short conv + SiLU, KDA step, gated RMSNorm
     kda_spec_decode        ragged speculative rows, T >= 1 tokens each
+    kda_spec_verify_decode the same from a read-only state, with commit caches
 
 Build the library with ``python -m linear_attention_decode_02_gb300.build``.
 """
@@ -13,4 +14,4 @@ Build the library with ``python -m linear_attention_decode_02_gb300.build``.
 from .binding import (SCHED_AUTO, SCHED_SPLIT, SCHED_STREAM, KdaError, kda_device_error,  # noqa: F401
                       kda_fused_decode, kda_packed_decode, kda_plan_schedule, kda_plan_split,
                       kda_recurrent_decode, kda_set_schedule_override, kda_set_split_override,
-                      kda_spec_decode, kda_version, library)
+                      kda_spec_decode, kda_spec_verify_decode, kda_version, library)

@@ -30,6 +30,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(128.0)
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_recurrent_decode", "kda_packed_decode", "kda_fused_decode", "kda_spec_decode",
+           "kda_spec_verify_decode",
            "kda_plan_split", "kda_set_split_override", "kda_plan_schedule", "kda_set_schedule_override",
            "kda_device_error", "kda_selftest_wait_timeout", "kda_status_string", "kda_last_error_message",
            "kda_version")
@@ -57,6 +58,7 @@ def _declare(lib):
         "kda_packed_decode": [T, T, T, T, T, T, T, T, vp],
         "kda_fused_decode": [T, T, T, T, T, T, T, T, T, T, T, i32, f32, f32, T, vp],
         "kda_spec_decode": [T, T, T, T, T, i32, T, i32, T, T, T, f32, vp],
+        "kda_spec_verify_decode": [T, T, T, T, T, i32, T, i32, T, T, T, T, T, f32, vp],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -182,6 +184,22 @@ def kda_spec_decode(q, k, v, g, beta, cu_seqlens, state_indices, state, t_max, o
         st = lib.kda_spec_decode(_ref(q), _ref(k), _ref(v), _ref(g), _ref(beta), int(bool(beta_is_logit)),
                                  _ref(cu_seqlens), int(t_max), _ref(state_indices), _ref(state),
                                  _ref(out), float(scale), _stream(q))
+    _check(lib, st)
+    return out
+
+
+def kda_spec_verify_decode(q, k, v, g, beta, cu_seqlens, state_indices, state, t_max, out=None,
+                           correction_cache=None, kg_cache=None, beta_is_logit=True, scale=DEFAULT_SCALE):
+    """Speculative verify: spec outputs from a read-only state, optional commit caches."""
+    lib = library()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    cc = _ref(correction_cache) if correction_cache is not None else None
+    kg = _ref(kg_cache) if kg_cache is not None else None
+    with torch.cuda.device(q.device):
+        st = lib.kda_spec_verify_decode(_ref(q), _ref(k), _ref(v), _ref(g), _ref(beta), int(bool(beta_is_logit)),
+                                        _ref(cu_seqlens), int(t_max), _ref(state_indices), _ref(state), _ref(out),
+                                        cc, kg, float(scale), _stream(q))
     _check(lib, st)
     return out
 

@@ -574,11 +574,18 @@ kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, 
   return check_launch(kda::launch_fused(a, S.dtype, st));
 }
 
-kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
-                           const kda_tensor* beta, int32_t beta_is_logit, const kda_tensor* cu_seqlens,
-                           int32_t t_max, const kda_tensor* state_indices, const kda_tensor* state,
-                           const kda_tensor* out, float scale, void* stream) {
-  View Q, K, V, Gt, Bt, CU, I, S, O;
+}  // extern "C"
+
+namespace {
+
+// Shared by kda_spec_decode and kda_spec_verify_decode.  corr / kg are
+// validated only in verify mode (either may be null there).
+kda_status spec_common(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
+                       const kda_tensor* beta, int32_t beta_is_logit, const kda_tensor* cu_seqlens, int32_t t_max,
+                       const kda_tensor* state_indices, const kda_tensor* state, const kda_tensor* out,
+                       const kda_tensor* correction_cache, const kda_tensor* kg_cache, bool verify, float scale,
+                       void* stream) {
+  View Q, K, V, Gt, Bt, CU, I, S, O, CC, KG;
   KDA_TRY(ranked_view(q, "q", 3, -1, &Q));
   KDA_TRY(ranked_view(k, "k", 3, -1, &K));
   KDA_TRY(ranked_view(v, "v", 3, -1, &V));
@@ -620,7 +627,31 @@ kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_t
   KDA_TRY(need_shape(O, 2, kD));
   KDA_CHECK(std::isfinite(scale) && scale > 0.f, KDA_ERR_INVALID_ARG, "scale must be finite and positive");
   KDA_TRY(no_alias(O, {&Q, &K, &V, &Gt, &Bt, &CU, &I, &S}));
-  KDA_TRY(no_alias(S, {&Q, &K, &V, &Gt, &Bt, &CU, &I}));
+  int64_t t_cap = 0;
+  if (verify) {
+    KDA_CHECK(t_max <= 16, KDA_ERR_UNSUPPORTED, "verify mode serves up to 16 tokens per row (t_max %d)", t_max);
+    for (const kda_tensor* c : {correction_cache, kg_cache}) {
+      if (c == nullptr) continue;
+      View* w = c == correction_cache ? &CC : &KG;
+      KDA_TRY(raw_view(c, c == correction_cache ? "correction_cache" : "kg_cache", w));
+      KDA_TRY(need_dtype(*w, KDA_F32));
+      KDA_CHECK(w->ndim == 4, KDA_ERR_INVALID_ARG, "%s: expected rank 4", w->name);
+      KDA_TRY(need_shape(*w, 0, S.shape[0]));
+      KDA_TRY(need_shape(*w, 1, H));
+      KDA_TRY(need_shape(*w, 3, c == correction_cache ? kD : 2 * kD));
+      KDA_CHECK(w->shape[2] >= 1 && w->shape[2] <= 16, KDA_ERR_INVALID_ARG, "%s: token capacity %lld not in 1..16",
+                w->name, (long long)w->shape[2]);
+      KDA_CHECK(t_cap == 0 || w->shape[2] == t_cap, KDA_ERR_INVALID_ARG, "caches disagree on the token capacity");
+      t_cap = w->shape[2];
+      KDA_TRY(need_contiguous(*w));
+      KDA_CHECK(reinterpret_cast<uintptr_t>(w->data) % 16 == 0, KDA_ERR_INVALID_ARG, "%s: data must be 16-byte aligned",
+                w->name);
+      KDA_TRY(no_alias(*w, {&Q, &K, &V, &Gt, &Bt, &CU, &I, &S, &O}));
+    }
+    if (correction_cache != nullptr && kg_cache != nullptr) KDA_TRY(no_alias(CC, {&KG}));
+  } else {
+    KDA_TRY(no_alias(S, {&Q, &K, &V, &Gt, &Bt, &CU, &I}));
+  }
   if (R == 0) return KDA_OK;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -644,7 +675,32 @@ kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_t
   a.state = S.data; a.slot_stride = S.stride[0]; a.num_slots = (int32_t)S.shape[0];
   a.out = O.data; a.N = (int32_t)N; a.R = (int32_t)R; a.H = (int32_t)H;
   a.scale = scale;
-  return check_launch(kda::launch_spec(a, S.dtype, split, st));
+  a.corr = verify && correction_cache != nullptr ? reinterpret_cast<float*>(CC.data) : nullptr;
+  a.kg = verify && kg_cache != nullptr ? reinterpret_cast<float*>(KG.data) : nullptr;
+  a.t_cap = (int32_t)t_cap;
+  return check_launch(kda::launch_spec(a, S.dtype, split, verify, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+kda_status kda_spec_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v, const kda_tensor* g,
+                           const kda_tensor* beta, int32_t beta_is_logit, const kda_tensor* cu_seqlens,
+                           int32_t t_max, const kda_tensor* state_indices, const kda_tensor* state,
+                           const kda_tensor* out, float scale, void* stream) {
+  return spec_common(q, k, v, g, beta, beta_is_logit, cu_seqlens, t_max, state_indices, state, out, nullptr,
+                     nullptr, false, scale, stream);
+}
+
+kda_status kda_spec_verify_decode(const kda_tensor* q, const kda_tensor* k, const kda_tensor* v,
+                                  const kda_tensor* g, const kda_tensor* beta, int32_t beta_is_logit,
+                                  const kda_tensor* cu_seqlens, int32_t t_max, const kda_tensor* state_indices,
+                                  const kda_tensor* state, const kda_tensor* out,
+                                  const kda_tensor* correction_cache, const kda_tensor* kg_cache, float scale,
+                                  void* stream) {
+  return spec_common(q, k, v, g, beta, beta_is_logit, cu_seqlens, t_max, state_indices, state, out,
+                     correction_cache, kg_cache, true, scale, stream);
 }
 
 int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max, int32_t sm_count) {

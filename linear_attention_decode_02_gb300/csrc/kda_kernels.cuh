@@ -383,11 +383,14 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
 // decays are clamped at -60: anything decayed further is below float32
 // resolution of the rest of the row).
 // Grid slice n == N zeroes the padding token rows outside [cu[0], cu[N]).
+// VERIFY: the state is read-only (never stored); token position t < t_cap of
+// a live row records its correction u_t and its raw key | log decay in the
+// optional slot-indexed caches.
 // =====================================================================================
 constexpr float kSpecMaxLogDecay = 80.f;   // chunk bound on the summed per-token decay
 constexpr float kSpecLogDecayFloor = -60.f;
 
-template <typename StateT, int CW, int NW>
+template <typename StateT, int CW, int NW, bool VERIFY>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel(const SpecArgs a) {
   using G = Strip<StateT, CW>;
   constexpr int SPLIT = kD / (CW * NW);
@@ -442,6 +445,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
       reinterpret_cast<float4*>(s_v[j])[lane] =
           load4(a.v, (int64_t)t * a.v_rs + (int64_t)h * a.v_hs + 4 * lane, a.qkv_dtype);
       float4 g = __ldg(reinterpret_cast<const float4*>(a.g + (int64_t)t * a.g_rs + (int64_t)h * a.g_hs + 4 * lane));
+      if (VERIFY && a.kg != nullptr && split == 0 && t - t0 < a.t_cap) {
+        float* kgp = a.kg + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * (2 * kD);
+        reinterpret_cast<float4*>(kgp)[lane] = k;
+        reinterpret_cast<float4*>(kgp + kD)[lane] = g;
+      }
       g = make_float4(fmaxf(g.x, kSpecLogDecayFloor), fmaxf(g.y, kSpecLogDecayFloor),
                       fmaxf(g.z, kSpecLogDecayFloor), fmaxf(g.w, kSpecLogDecayFloor));
       float qq = q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
@@ -500,6 +508,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
         u[jj] = tk.x * (vv[jj] - acc_a[jj]);
         o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
       }
+      if (VERIFY && a.corr != nullptr && row0 == 0 && t - t0 < a.t_cap) {
+        float* cp = a.corr + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * kD + col0;
+#pragma unroll
+        for (int jj = 0; jj < G::VEC; jj += 4)
+          *reinterpret_cast<float4*>(cp + jj) = make_float4(u[jj], u[jj + 1], u[jj + 2], u[jj + 3]);
+      }
       // S~ += (k / P_t) u^T
       float2 u2[G::VEC / 2];
       pairs_of<G::VEC>(u, u2);
@@ -521,7 +535,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
     }
     tc0 += ne;
   }
-  strip_store<StateT, G>(sp, row0, col0, S);
+  if (!VERIFY) strip_store<StateT, G>(sp, row0, col0, S);
 }
 
 }  // namespace kda

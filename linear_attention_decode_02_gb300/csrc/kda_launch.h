@@ -61,12 +61,16 @@ struct SpecArgs {
   void* out;                              // bf16 [R, H, 128]
   int32_t N, R, H;
   float scale;
+  // verify mode (state read-only): optional slot-indexed caches, contiguous
+  float* corr;                            // [num_slots, H, t_cap, 128] u_t
+  float* kg;                              // [num_slots, H, t_cap, 256] raw k | g
+  int32_t t_cap;
 };
 
 // Launchers: return the launch error (cudaSuccess on success).
 cudaError_t launch_t1(const T1Args& a, int state_dtype, int split, cudaStream_t s);
 cudaError_t launch_fused(const FusedArgs& a, int state_dtype, cudaStream_t s);
-cudaError_t launch_spec(const SpecArgs& a, int state_dtype, int split, cudaStream_t s);
+cudaError_t launch_spec(const SpecArgs& a, int state_dtype, int split, bool verify, cudaStream_t s);
 
 // Persistent streaming T=1 kernel (bulk copies into shared-memory stages);
 // needs 16-byte aligned q / k / v / gate head vectors.

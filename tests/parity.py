@@ -162,3 +162,26 @@ def assert_untouched(before, after, touched_slots):
 
 def live_slots(idx, num_slots):
     return sorted({int(s) for s in idx.tolist() if 0 < int(s) < num_slots})
+
+
+def oracle_verify(case, t_cap, rows=None, beta_is_logit=True, scale=ko.SCALE):
+    """Oracle verify mode over the sequences `rows`:
+    ({token_row: out [H,128]}, {slot: corr [H,t_cap,128]}, {slot: kg [H,t_cap,256]})."""
+    idx = case["state_indices"].numpy()
+    cu = case["cu_seqlens"].numpy()
+    N = idx.shape[0]
+    rows = list(range(N)) if rows is None else list(rows)
+    slots, remap, sub_idx = _compact(idx, case["state"].shape[0], rows)
+    R = case["q"].shape[0]
+    tok, sub_cu = [], [0]
+    for n in rows:
+        t0, t1 = max(int(cu[n]), 0), min(int(cu[n + 1]), R)
+        ts = list(range(t0, t1)) if t1 > t0 else []
+        tok += ts
+        sub_cu.append(sub_cu[-1] + len(ts))
+    t = torch.tensor(tok, dtype=torch.long)
+    out, corr, kg = ko.spec_verify(f64(case["q"][t]), f64(case["k"][t]), f64(case["v"][t]), f64(case["g"][t]),
+                                   f64(case["beta"][t]), np.array(sub_cu), sub_idx, _pool(case["state"], slots),
+                                   t_cap, beta_is_logit=beta_is_logit, scale=scale)
+    return ({tr: out[i] for i, tr in enumerate(tok)}, {s: corr[remap[s]] for s in slots},
+            {s: kg[remap[s]] for s in slots})

@@ -268,6 +268,38 @@ def test_spec_contract(lib):
     assert _call_spec(lib, t) == OK  # no token rows: nothing to launch
 
 
+def _call_verify(lib, t, corr=None, kg=None, t_max=3):
+    d = {n: ctypes.byref(desc(v)) for n, v in t.items()}
+    c = ctypes.byref(desc(corr)) if corr is not None else None
+    g = ctypes.byref(desc(kg)) if kg is not None else None
+    return lib.kda_spec_verify_decode(d["q"], d["k"], d["v"], d["g"], d["beta"], 1, d["cu_seqlens"], t_max,
+                                      d["state_indices"], d["state"], d["out"], c, g, 0.088, None)
+
+
+def test_spec_verify_contract(lib):
+    M, H = 12, 2
+    if NO_GPU:
+        assert _passes_validation(_call_verify(lib, _spec_args())), _msg(lib)
+        assert _passes_validation(_call_verify(lib, _spec_args(), torch.zeros(M, H, 4, 128),
+                                               torch.zeros(M, H, 4, 256))), _msg(lib)
+    assert _call_verify(lib, _spec_args(), t_max=17) == UNSUPPORTED
+    assert _call_verify(lib, _spec_args(), torch.zeros(M, H, 4, 128), torch.zeros(M, H, 5, 256)) == INVALID
+    assert "token capacity" in _msg(lib)
+    assert _call_verify(lib, _spec_args(), torch.zeros(M, H, 17, 128)) == INVALID
+    assert _call_verify(lib, _spec_args(), torch.zeros(M + 1, H, 4, 128)) == INVALID
+    assert _call_verify(lib, _spec_args(), None, torch.zeros(M, H, 4, 128)) == INVALID
+    assert _call_verify(lib, _spec_args(), torch.zeros(M, H, 4, 128, dtype=torch.bfloat16)) == INVALID
+    assert _call_verify(lib, _spec_args(), torch.zeros(M, H, 128, 4).transpose(2, 3)) == INVALID
+    both = torch.zeros(M, H, 4, 384)
+    assert _call_verify(lib, _spec_args(), both[..., :128], both[..., 128:]) == INVALID  # not contiguous
+    buf = torch.zeros(M * H * 4 * 256)
+    assert _call_verify(lib, _spec_args(), buf[: M * H * 4 * 128].view(M, H, 4, 128),
+                        buf.view(M, H, 4, 256)) == ALIAS
+    t = _spec_args()
+    flat = t["state"].view(-1)
+    assert _call_verify(lib, t, flat[: M * H * 4 * 128].view(M, H, 4, 128)) == ALIAS
+
+
 def test_schedule_override_and_plan(lib):
     assert lib.kda_set_schedule_override(7) == INVALID
     assert lib.kda_set_schedule_override(2) == OK
