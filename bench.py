@@ -31,6 +31,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -95,6 +96,18 @@ def _slot_sets(n_sets, count, num_slots, null_count, seed, null_values=(-1,)):
     return sets
 
 
+SPLIT_SOURCE = {0: "kda_t1.cu", 1: "kda_t1.cu", 2: "kda_fused.cu", 3: "kda_spec.cu"}
+
+
+def kernel_source(op, units, state_dtype):
+    """Translation unit of the kernel the library's dispatch picks for this call shape."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    code = 0 if state_dtype == torch.float32 else 1
+    if binding.kda_plan_schedule(op, units, code, 1, sms) == binding.SCHED_STREAM:
+        return "kda_stream.cu"
+    return SPLIT_SOURCE[op]
+
+
 class Workload:
     """One decode path at one size: device inputs, a call per step, its byte model."""
 
@@ -123,6 +136,7 @@ class Recurrent(Workload):
                            state="float32" if esz == 4 else "bfloat16", activations="bfloat16",
                            gate="softplus" if lower_bound is None else f"lower_bound {lower_bound}")
         self.e2e_keys = ("q", "k", "v", "raw_gate", "raw_beta")
+        self.source = kernel_source(0, B * H, state_dtype)
 
     def call(self, idx):
         d = self.d
@@ -143,6 +157,7 @@ class Packed(Workload):
         self.config = dict(workload="packed_kimi_k3_t1", H=12, B=B, num_slots=slots, state="bfloat16",
                            padding_rows=nn, gate="lower_bound -5")
         self.e2e_keys = ("mixed_qkv", "raw_gate", "raw_beta")
+        self.source = kernel_source(1, B * 12, torch.bfloat16)
 
     def call(self, idx):
         d = self.d
@@ -170,6 +185,7 @@ class Fused(Workload):
                            state="float32" if state_dtype == torch.float32 else "bfloat16", null_rows=nn,
                            gate=f"lower_bound {lower_bound}" if lower_bound is not None else "softplus")
         self.e2e_keys = ("x", "raw_gate", "raw_beta", "output_gate")
+        self.source = kernel_source(2, rows * H, state_dtype)
 
     def call(self, idx):
         d = self.d
@@ -197,6 +213,7 @@ class Spec(Workload):
                            empty_rows=N - live_rows, num_slots=slots,
                            state="float32" if state_dtype == torch.float32 else "bfloat16",
                            gates="precomputed fp32 log decay in [-5, 0]")
+        self.source = kernel_source(3, N * H, state_dtype)
         self.e2e_keys = ("q", "k", "v", "g", "beta", "cu_seqlens")
 
     def call(self, idx):
@@ -225,28 +242,42 @@ def measured_peaks():
         return None
 
 
-def kernel_source_hash():
-    """Hash of the device-code sources (the host dispatcher kda_api.cu excluded)."""
+CSRC = os.path.join(ROOT, "linear_attention_decode_02_gb300", "csrc")
+
+
+def source_closure(name):
+    """`name` and every csrc file it includes, transitively (quoted includes only)."""
+    seen, todo = [], [name]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(os.path.join(CSRC, f)):
+            continue
+        seen.append(f)
+        with open(os.path.join(CSRC, f)) as fh:
+            todo += re.findall(r'^#include\s+"([^"/]+)"', fh.read(), re.M)
+    return sorted(seen)
+
+
+def kernel_source_hash(name="kda_t1.cu"):
+    """Hash of one kernel translation unit and the csrc headers it includes."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "linear_attention_decode_02_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")) and name != "kda_api.cu":
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for f in source_closure(name):
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kind):
-    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged since."""
+    """DRAM bytes per launch from the committed ncu summary, if that kernel's sources are unchanged since."""
     try:
         with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
             rec = json.load(f)
     except (OSError, ValueError):
         return None
-    if rec.get("source_hash") != kernel_source_hash():
-        return None
     entry = rec.get("kernels", {}).get(kind)
-    return entry.get("dram_bytes_per_launch") if entry else None
+    if not entry or entry.get("source_hash") != kernel_source_hash(entry.get("source", "")):
+        return None
+    return entry.get("dram_bytes_per_launch")
 
 
 class ClockSampler:
@@ -576,7 +607,7 @@ def main():
         e_max = max_over_ranks(e_ms)
         e2e_obj = {"value": round(job_gbs(wl.nbytes, world, e_max), 1), "unit": "GB/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_max, 5)}
-    name, cfg, nbytes = wl.name, dict(wl.config), wl.nbytes
+    name, cfg, nbytes, source = wl.name, dict(wl.config), wl.nbytes, wl.source
     del wl
     torch.cuda.empty_cache()
 
@@ -605,7 +636,7 @@ def main():
                          "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name), "kernel": name,
                          "peak_source": f"{peak_src} copy bandwidth (burst)"},
             "e2e": e2e_obj, "clocks": clocks.summary(w0, w1), "cpu_baseline": cpu, "paths": paths,
-            "kernel_source_hash": kernel_source_hash(),
+            "kernel_source": source, "kernel_source_hash": kernel_source_hash(source),
         }
         print(json.dumps(line))
     if dist is not None:

@@ -1,4 +1,4 @@
-// KDA decode kernels for sm_103a.
+// Register-strip building blocks of the KDA decode kernels for sm_103a.
 //
 // Work decomposition.  For one (row, head) unit the value columns of the
 // 128 x 128 state S[k][v] update independently:
@@ -195,347 +195,5 @@ template <int NW>
 struct MinBlocks {
   static constexpr int value = NW >= 16 ? 1 : 16 / NW;
 };
-
-// =====================================================================================
-// T=1: one CTA per (row, head, split); NW warps x CW columns = 128/split columns.
-// =====================================================================================
-template <typename StateT, int CW, int NW>
-__global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_t1_kernel(const T1Args a) {
-  using G = Strip<StateT, CW>;
-  constexpr int SPLIT = kD / (CW * NW);
-  static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
-  __shared__ float4 s_coef[NW][kD];
-
-  const int split = blockIdx.x % SPLIT;
-  const int unit = blockIdx.x / SPLIT;
-  const int h = unit % a.H;
-  const int b = unit / a.H;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int col0 = (split * NW + warp) * CW + (lane % G::LPR) * G::VEC;
-  const int row0 = lane / G::LPR;
-  const int c4 = lane * 4;
-
-  // Activation loads first: they do not depend on the slot.
-  const float4 q = load4(a.q, (int64_t)b * a.q_rs + (int64_t)h * a.q_hs + c4, a.qkv_dtype);
-  const float4 k = load4(a.k, (int64_t)b * a.k_rs + (int64_t)h * a.k_hs + c4, a.qkv_dtype);
-  const float4 gr = load4(a.gate, (int64_t)b * a.g_rs + (int64_t)h * a.g_hs + c4, a.gate_dtype);
-  const float4 dtb = __ldg(reinterpret_cast<const float4*>(a.dt_bias + h * kD + c4));
-  const float A = expf(__ldg(a.A_log + h));
-  const float braw = load1(a.beta, (int64_t)b * a.b_rs + (int64_t)h * a.b_hs, a.beta_dtype);
-  float vv[G::VEC];
-  load_cols<G::VEC>(a.v, (int64_t)b * a.v_rs + (int64_t)h * a.v_hs + col0, a.qkv_dtype, vv);
-
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)b * a.H + h) * kD;
-  const int slot = __ldg(a.idx + b);
-  if (slot <= 0 || slot >= a.num_slots) {  // null row: zero output, no cache access
-    if (row0 == 0) store_out_zero<G::VEC>(out + col0);
-    return;
-  }
-
-  StateT* sp = static_cast<StateT*>(a.state) + (int64_t)slot * a.slot_stride + (int64_t)h * kD * kD;
-  RawRegs<StateT, G> S;
-  strip_load<StateT, G>(sp, row0, col0, S);
-
-  float4 d;
-  d.x = expf(log_decay(gr.x + dtb.x, A, a.gate_mode, a.lower_bound));
-  d.y = expf(log_decay(gr.y + dtb.y, A, a.gate_mode, a.lower_bound));
-  d.z = expf(log_decay(gr.z + dtb.z, A, a.gate_mode, a.lower_bound));
-  d.w = expf(log_decay(gr.w + dtb.w, A, a.gate_mode, a.lower_bound));
-  float4* coef = s_coef[warp];
-  const float qk = token_coefficients(q, k, d, lane, coef);
-  const float beta = sigmoidf_(braw);
-  __syncwarp();
-
-  float acc_a[G::VEC], acc_b[G::VEC];
-  strip_reduce<G>(S, coef, row0, acc_a, acc_b);
-  float u[G::VEC], o[G::VEC];
-#pragma unroll
-  for (int j = 0; j < G::VEC; ++j) {
-    u[j] = beta * (vv[j] - acc_a[j]);
-    o[j] = a.scale * (acc_b[j] + qk * u[j]);
-  }
-  strip_update_store<StateT, G>(sp, row0, col0, S, coef, u);
-  if (row0 == 0) store_out<G::VEC>(out + col0, o);
-}
-
-// =====================================================================================
-// Fused conv + SiLU + KDA + gated RMSNorm: one CTA of 8 warps per (row, head).
-// =====================================================================================
-template <typename StateT>
-__global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
-  constexpr int CW = 16, NW = 8, NT = NW * 32;
-  using G = Strip<StateT, CW>;
-  static_assert(CW * NW == kD, "one CTA covers all value columns");
-  __shared__ float s_a[3 * kD];  // SiLU(conv) of this head's q | k | v channels
-  __shared__ float s_d[kD];      // decay exp(g)
-  __shared__ float4 s_coef[NW][kD];
-  __shared__ float s_ss[NW];
-
-  const int unit = blockIdx.x;
-  const int h = unit % a.H;
-  const int r = unit / a.H;
-  const int tid = threadIdx.x;
-  const int warp = tid >> 5;
-  const int lane = tid & 31;
-  const int col0 = warp * CW + (lane % G::LPR) * G::VEC;
-  const int row0 = lane / G::LPR;
-
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)r * a.H + h) * kD;
-  const int slot = __ldg(a.idx + r);
-  if (slot <= 0 || slot >= a.num_slots) {  // null row: zero output, neither cache touched
-    if (row0 == 0) store_out_zero<G::VEC>(out + col0);
-    return;
-  }
-
-  StateT* sp = static_cast<StateT*>(a.state) + (int64_t)slot * a.slot_stride + (int64_t)h * kD * kD;
-  RawRegs<StateT, G> S;
-  strip_load<StateT, G>(sp, row0, col0, S);
-
-  // Short conv over [cache0, cache1, cache2, x] (oldest first) for the 384
-  // channels of this head, then the cache shift.  Each channel is read and
-  // written by the same thread; heads own disjoint channels.
-  const int HD = a.H * kD;
-  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(a.x) + (int64_t)r * a.x_rs;
-  __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state) + (int64_t)slot * a.cs_slot_stride;
-  for (int lc = tid; lc < 3 * kD; lc += NT) {
-    const int sec = lc >> 7;
-    const int ch = sec * HD + h * kD + (lc & (kD - 1));
-    const __nv_bfloat16 xb = xr[ch];
-    __nv_bfloat16* cp = cs + ch;
-    const __nv_bfloat16 c0 = cp[0];
-    const __nv_bfloat16 c1 = cp[a.cs_tap_stride];
-    const __nv_bfloat16 c2 = cp[2 * a.cs_tap_stride];
-    const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + (lc & (kD - 1));
-    float y = __ldg(w) * __bfloat162float(c0);
-    y = fmaf(__ldg(w + HD), __bfloat162float(c1), y);
-    y = fmaf(__ldg(w + 2 * HD), __bfloat162float(c2), y);
-    y = fmaf(__ldg(w + 3 * HD), __bfloat162float(xb), y);
-    s_a[lc] = y * sigmoidf_(y);
-    cp[0] = c1;
-    cp[a.cs_tap_stride] = c2;
-    cp[2 * a.cs_tap_stride] = xb;
-  }
-  if (tid < kD) {
-    const float A = expf(__ldg(a.A_log + h));
-    const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(a.gate)[(int64_t)r * a.g_rs +
-                                                                                (int64_t)h * a.g_hs + tid]) +
-                    __ldg(a.dt_bias + h * kD + tid);
-    s_d[tid] = expf(log_decay(x, A, a.gate_mode, a.lower_bound));
-  }
-  const float beta = sigmoidf_(
-      __bfloat162float(static_cast<const __nv_bfloat16*>(a.beta)[(int64_t)r * a.b_rs + (int64_t)h * a.b_hs]));
-  // Epilogue operands, loaded early.
-  float nw[G::VEC], og[G::VEC];
-#pragma unroll
-  for (int j = 0; j < G::VEC; ++j) nw[j] = __ldg(a.norm_w + col0 + j);
-  load_cols<G::VEC>(a.out_gate, (int64_t)r * a.og_rs + (int64_t)h * a.og_hs + col0, KDA_DT_BF16, og);
-  __syncthreads();
-
-  const float4 q = *reinterpret_cast<const float4*>(s_a + 4 * lane);
-  const float4 k = *reinterpret_cast<const float4*>(s_a + kD + 4 * lane);
-  const float4 d = *reinterpret_cast<const float4*>(s_d + 4 * lane);
-  float4* coef = s_coef[warp];
-  const float qk = token_coefficients(q, k, d, lane, coef);
-  float vv[G::VEC];
-#pragma unroll
-  for (int j = 0; j < G::VEC; ++j) vv[j] = s_a[2 * kD + col0 + j];
-  __syncwarp();
-
-  float acc_a[G::VEC], acc_b[G::VEC];
-  strip_reduce<G>(S, coef, row0, acc_a, acc_b);
-  float u[G::VEC], o[G::VEC];
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < G::VEC; ++j) {
-    u[j] = beta * (vv[j] - acc_a[j]);
-    o[j] = a.scale * (acc_b[j] + qk * u[j]);
-    ss = fmaf(o[j], o[j], ss);
-  }
-  strip_update_store<StateT, G>(sp, row0, col0, S, coef, u);
-
-  // Gated RMSNorm over the 128 value columns: lanes with row0 == 0 hold
-  // distinct columns; one barrier to combine the 8 warps.
-  ss = warp_sum(row0 == 0 ? ss : 0.f);
-  if (lane == 0) s_ss[warp] = ss;
-  __syncthreads();
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) tot += s_ss[w];
-  const float rinv = rsqrtf(tot * (1.f / kD) + a.norm_eps);
-  if (row0 == 0) {
-    float y[G::VEC];
-#pragma unroll
-    for (int j = 0; j < G::VEC; ++j) y[j] = o[j] * rinv * nw[j] * sigmoidf_(og[j]);
-    store_out<G::VEC>(out + col0, y);
-  }
-}
-
-// =====================================================================================
-// Speculative T >= 1: one CTA per (row, head, split); the state stays in
-// float32 registers across the row's tokens.  Tokens are staged TC at a
-// time.  Within a chunk the decay is deferred: with P_t the cumulative decay
-// of each key row since the chunk start, the registers hold S~ = S / P_t, so
-// the reductions use (P_t k, P_t q) and the update is one paired FMA,
-// S~ += (k / P_t) u^T; the true state P_end S~ is restored at chunk end.  A
-// chunk ends early once the sum over its tokens of the largest per-row decay
-// exceeds e^-80, keeping P_t and 1/P_t finite in float32 (per-element log
-// decays are clamped at -60: anything decayed further is below float32
-// resolution of the rest of the row).
-// Grid slice n == N zeroes the padding token rows outside [cu[0], cu[N]).
-// VERIFY: the state is read-only (never stored); token position t < t_cap of
-// a live row records its correction u_t and its raw key | log decay in the
-// optional slot-indexed caches.
-// =====================================================================================
-constexpr float kSpecMaxLogDecay = 80.f;   // chunk bound on the summed per-token decay
-constexpr float kSpecLogDecayFloor = -60.f;
-
-template <typename StateT, int CW, int NW, bool VERIFY>
-__global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel(const SpecArgs a) {
-  using G = Strip<StateT, CW>;
-  constexpr int SPLIT = kD / (CW * NW);
-  constexpr int TC = 8;
-  constexpr int NT = NW * 32;
-  static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
-  __shared__ float4 s_coef[TC][kD];  // staged (q, k, g), then (P k, P q, k / P, k / P)
-  __shared__ float4 s_tok[TC];       // (beta, q.k, largest per-row decay, -)
-  __shared__ float s_P[kD];          // P at the chunk end, per key row
-  __shared__ __align__(16) float s_v[TC][kD];  // the chunk's value vectors
-
-  const int split = blockIdx.x % SPLIT;
-  const int unit = blockIdx.x / SPLIT;
-  const int h = unit % a.H;
-  const int n = unit / a.H;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int col0 = (split * NW + warp) * CW + (lane % G::LPR) * G::VEC;
-  const int row0 = lane / G::LPR;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD + col0;
-  const int64_t out_rs = (int64_t)a.H * kD;
-
-  if (n == a.N) {  // padding token rows
-    const int lo = min(max(__ldg(a.cu), 0), a.R);
-    const int hi = max(min(__ldg(a.cu + a.N), a.R), lo);
-    for (int t = row0; t < lo; t += G::RPI) store_out_zero<G::VEC>(out + t * out_rs);
-    for (int t = hi + row0; t < a.R; t += G::RPI) store_out_zero<G::VEC>(out + t * out_rs);
-    return;
-  }
-
-  const int t0 = max(__ldg(a.cu + n), 0);
-  const int t1 = min(__ldg(a.cu + n + 1), a.R);
-  if (t1 <= t0) return;  // empty row
-  const int slot = __ldg(a.idx + n);
-  if (slot <= 0 || slot >= a.num_slots) {  // null row: zero its token rows
-    for (int t = t0 + row0; t < t1; t += G::RPI) store_out_zero<G::VEC>(out + t * out_rs);
-    return;
-  }
-
-  StateT* sp = static_cast<StateT*>(a.state) + (int64_t)slot * a.slot_stride + (int64_t)h * kD * kD;
-  FltRegs<G> S;
-  strip_load<StateT, G>(sp, row0, col0, S);
-
-  for (int tc0 = t0; tc0 < t1;) {
-    const int nt = min(TC, t1 - tc0);
-    if (tc0 != t0) __syncthreads();  // previous chunk fully consumed
-    // per-token prologue, one token per warp: normalised q, k and the log decay
-    for (int j = warp; j < nt; j += NW) {
-      const int t = tc0 + j;
-      const float4 q = load4(a.q, (int64_t)t * a.q_rs + (int64_t)h * a.q_hs + 4 * lane, a.qkv_dtype);
-      const float4 k = load4(a.k, (int64_t)t * a.k_rs + (int64_t)h * a.k_hs + 4 * lane, a.qkv_dtype);
-      reinterpret_cast<float4*>(s_v[j])[lane] =
-          load4(a.v, (int64_t)t * a.v_rs + (int64_t)h * a.v_hs + 4 * lane, a.qkv_dtype);
-      float4 g = __ldg(reinterpret_cast<const float4*>(a.g + (int64_t)t * a.g_rs + (int64_t)h * a.g_hs + 4 * lane));
-      if (VERIFY && a.kg != nullptr && split == 0 && t - t0 < a.t_cap) {
-        float* kgp = a.kg + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * (2 * kD);
-        reinterpret_cast<float4*>(kgp)[lane] = k;
-        reinterpret_cast<float4*>(kgp + kD)[lane] = g;
-      }
-      g = make_float4(fmaxf(g.x, kSpecLogDecayFloor), fmaxf(g.y, kSpecLogDecayFloor),
-                      fmaxf(g.z, kSpecLogDecayFloor), fmaxf(g.w, kSpecLogDecayFloor));
-      float qq = q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
-      float kk = k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w;
-      float qk = q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w;
-      float gm = fmaxf(fmaxf(-g.x, -g.y), fmaxf(-g.z, -g.w));
-      qq = warp_sum(qq);
-      kk = warp_sum(kk);
-      qk = warp_sum(qk);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
-      const float rq = rsqrtf(qq + kL2Eps), rk = rsqrtf(kk + kL2Eps);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        s_coef[j][4 * lane + i] = make_float4(f4get(q, i) * rq, f4get(k, i) * rk, f4get(g, i), 0.f);
-      if (lane == 0) {
-        const float braw = load1(a.beta, (int64_t)t * a.b_rs + (int64_t)h * a.b_hs, a.beta_dtype);
-        s_tok[j] = make_float4(a.beta_is_logit ? sigmoidf_(braw) : braw, qk * rq * rk, gm, 0.f);
-      }
-    }
-    __syncthreads();
-    // tokens of this chunk: the longest prefix whose summed decay stays within the bound
-    int ne = 1;
-    {
-      float acc = s_tok[0].z;
-      for (int j = 1; j < nt; ++j) {
-        acc += s_tok[j].z;
-        if (acc > kSpecMaxLogDecay) break;
-        ne = j + 1;
-      }
-    }
-    // cumulative decay per key row -> deferred-decay coefficients
-    for (int r = threadIdx.x; r < kD; r += NT) {
-      float Gs = 0.f, P = 1.f;
-      for (int j = 0; j < ne; ++j) {
-        const float4 c = s_coef[j][r];  // (q, k, g, -)
-        Gs += c.z;
-        P = expf(Gs);
-        const float ku = c.y * expf(-Gs);
-        s_coef[j][r] = make_float4(P * c.y, P * c.x, ku, ku);
-      }
-      s_P[r] = P;
-    }
-    __syncthreads();
-    for (int j = 0; j < ne; ++j) {
-      const int t = tc0 + j;
-      float vv[G::VEC];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = s_v[j][col0 + jj];
-      const float4 tk = s_tok[j];
-      float acc_a[G::VEC], acc_b[G::VEC];
-      strip_reduce<G>(S, s_coef[j], row0, acc_a, acc_b);
-      float u[G::VEC], o[G::VEC];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) {
-        u[jj] = tk.x * (vv[jj] - acc_a[jj]);
-        o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
-      }
-      if (VERIFY && a.corr != nullptr && row0 == 0 && t - t0 < a.t_cap) {
-        float* cp = a.corr + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * kD + col0;
-#pragma unroll
-        for (int jj = 0; jj < G::VEC; jj += 4)
-          *reinterpret_cast<float4*>(cp + jj) = make_float4(u[jj], u[jj + 1], u[jj + 2], u[jj + 3]);
-      }
-      // S~ += (k / P_t) u^T
-      float2 u2[G::VEC / 2];
-      pairs_of<G::VEC>(u, u2);
-#pragma unroll
-      for (int i = 0; i < G::PASSES; ++i) {
-        const float4 c = s_coef[j][row0 + i * G::RPI];
-        const float2 ku = make_float2(c.z, c.w);
-#pragma unroll
-        for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = fma2(ku, u2[p], S.s[i][p]);
-      }
-      if (row0 == 0) store_out<G::VEC>(out + t * out_rs, o);
-    }
-    // restore the true state: S = P_end S~
-#pragma unroll
-    for (int i = 0; i < G::PASSES; ++i) {
-      const float2 pp = dup2(s_P[row0 + i * G::RPI]);
-#pragma unroll
-      for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = mul2(pp, S.s[i][p]);
-    }
-    tc0 += ne;
-  }
-  if (!VERIFY) strip_store<StateT, G>(sp, row0, col0, S);
-}
 
 }  // namespace kda

@@ -3,6 +3,173 @@
 
 namespace kda {
 
+// =====================================================================================
+// Speculative T >= 1: one CTA per (row, head, split); the state stays in
+// float32 registers across the row's tokens.  Tokens are staged TC at a
+// time.  Within a chunk the decay is deferred: with P_t the cumulative decay
+// of each key row since the chunk start, the registers hold S~ = S / P_t, so
+// the reductions use (P_t k, P_t q) and the update is one paired FMA,
+// S~ += (k / P_t) u^T; the true state P_end S~ is restored at chunk end.  A
+// chunk ends early once the sum over its tokens of the largest per-row decay
+// exceeds e^-80, keeping P_t and 1/P_t finite in float32 (per-element log
+// decays are clamped at -60: anything decayed further is below float32
+// resolution of the rest of the row).
+// Grid slice n == N zeroes the padding token rows outside [cu[0], cu[N]).
+// VERIFY: the state is read-only (never stored); token position t < t_cap of
+// a live row records its correction u_t and its raw key | log decay in the
+// optional slot-indexed caches.
+// =====================================================================================
+constexpr float kSpecMaxLogDecay = 80.f;   // chunk bound on the summed per-token decay
+constexpr float kSpecLogDecayFloor = -60.f;
+
+template <typename StateT, int CW, int NW, bool VERIFY>
+__global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel(const SpecArgs a) {
+  using G = Strip<StateT, CW>;
+  constexpr int SPLIT = kD / (CW * NW);
+  constexpr int TC = 8;
+  constexpr int NT = NW * 32;
+  static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
+  __shared__ float4 s_coef[TC][kD];  // staged (q, k, g), then (P k, P q, k / P, k / P)
+  __shared__ float4 s_tok[TC];       // (beta, q.k, largest per-row decay, -)
+  __shared__ float s_P[kD];          // P at the chunk end, per key row
+  __shared__ __align__(16) float s_v[TC][kD];  // the chunk's value vectors
+
+  const int split = blockIdx.x % SPLIT;
+  const int unit = blockIdx.x / SPLIT;
+  const int h = unit % a.H;
+  const int n = unit / a.H;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int col0 = (split * NW + warp) * CW + (lane % G::LPR) * G::VEC;
+  const int row0 = lane / G::LPR;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD + col0;
+  const int64_t out_rs = (int64_t)a.H * kD;
+
+  if (n == a.N) {  // padding token rows
+    const int lo = min(max(__ldg(a.cu), 0), a.R);
+    const int hi = max(min(__ldg(a.cu + a.N), a.R), lo);
+    for (int t = row0; t < lo; t += G::RPI) store_out_zero<G::VEC>(out + t * out_rs);
+    for (int t = hi + row0; t < a.R; t += G::RPI) store_out_zero<G::VEC>(out + t * out_rs);
+    return;
+  }
+
+  const int t0 = max(__ldg(a.cu + n), 0);
+  const int t1 = min(__ldg(a.cu + n + 1), a.R);
+  if (t1 <= t0) return;  // empty row
+  const int slot = __ldg(a.idx + n);
+  if (slot <= 0 || slot >= a.num_slots) {  // null row: zero its token rows
+    for (int t = t0 + row0; t < t1; t += G::RPI) store_out_zero<G::VEC>(out + t * out_rs);
+    return;
+  }
+
+  StateT* sp = static_cast<StateT*>(a.state) + (int64_t)slot * a.slot_stride + (int64_t)h * kD * kD;
+  FltRegs<G> S;
+  strip_load<StateT, G>(sp, row0, col0, S);
+
+  for (int tc0 = t0; tc0 < t1;) {
+    const int nt = min(TC, t1 - tc0);
+    if (tc0 != t0) __syncthreads();  // previous chunk fully consumed
+    // per-token prologue, one token per warp: normalised q, k and the log decay
+    for (int j = warp; j < nt; j += NW) {
+      const int t = tc0 + j;
+      const float4 q = load4(a.q, (int64_t)t * a.q_rs + (int64_t)h * a.q_hs + 4 * lane, a.qkv_dtype);
+      const float4 k = load4(a.k, (int64_t)t * a.k_rs + (int64_t)h * a.k_hs + 4 * lane, a.qkv_dtype);
+      reinterpret_cast<float4*>(s_v[j])[lane] =
+          load4(a.v, (int64_t)t * a.v_rs + (int64_t)h * a.v_hs + 4 * lane, a.qkv_dtype);
+      float4 g = __ldg(reinterpret_cast<const float4*>(a.g + (int64_t)t * a.g_rs + (int64_t)h * a.g_hs + 4 * lane));
+      if (VERIFY && a.kg != nullptr && split == 0 && t - t0 < a.t_cap) {
+        float* kgp = a.kg + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * (2 * kD);
+        reinterpret_cast<float4*>(kgp)[lane] = k;
+        reinterpret_cast<float4*>(kgp + kD)[lane] = g;
+      }
+      g = make_float4(fmaxf(g.x, kSpecLogDecayFloor), fmaxf(g.y, kSpecLogDecayFloor),
+                      fmaxf(g.z, kSpecLogDecayFloor), fmaxf(g.w, kSpecLogDecayFloor));
+      float qq = q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
+      float kk = k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w;
+      float qk = q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w;
+      float gm = fmaxf(fmaxf(-g.x, -g.y), fmaxf(-g.z, -g.w));
+      qq = warp_sum(qq);
+      kk = warp_sum(kk);
+      qk = warp_sum(qk);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+      const float rq = rsqrtf(qq + kL2Eps), rk = rsqrtf(kk + kL2Eps);
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        s_coef[j][4 * lane + i] = make_float4(f4get(q, i) * rq, f4get(k, i) * rk, f4get(g, i), 0.f);
+      if (lane == 0) {
+        const float braw = load1(a.beta, (int64_t)t * a.b_rs + (int64_t)h * a.b_hs, a.beta_dtype);
+        s_tok[j] = make_float4(a.beta_is_logit ? sigmoidf_(braw) : braw, qk * rq * rk, gm, 0.f);
+      }
+    }
+    __syncthreads();
+    // tokens of this chunk: the longest prefix whose summed decay stays within the bound
+    int ne = 1;
+    {
+      float acc = s_tok[0].z;
+      for (int j = 1; j < nt; ++j) {
+        acc += s_tok[j].z;
+        if (acc > kSpecMaxLogDecay) break;
+        ne = j + 1;
+      }
+    }
+    // cumulative decay per key row -> deferred-decay coefficients
+    for (int r = threadIdx.x; r < kD; r += NT) {
+      float Gs = 0.f, P = 1.f;
+      for (int j = 0; j < ne; ++j) {
+        const float4 c = s_coef[j][r];  // (q, k, g, -)
+        Gs += c.z;
+        P = expf(Gs);
+        const float ku = c.y * expf(-Gs);
+        s_coef[j][r] = make_float4(P * c.y, P * c.x, ku, ku);
+      }
+      s_P[r] = P;
+    }
+    __syncthreads();
+    for (int j = 0; j < ne; ++j) {
+      const int t = tc0 + j;
+      float vv[G::VEC];
+#pragma unroll
+      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = s_v[j][col0 + jj];
+      const float4 tk = s_tok[j];
+      float acc_a[G::VEC], acc_b[G::VEC];
+      strip_reduce<G>(S, s_coef[j], row0, acc_a, acc_b);
+      float u[G::VEC], o[G::VEC];
+#pragma unroll
+      for (int jj = 0; jj < G::VEC; ++jj) {
+        u[jj] = tk.x * (vv[jj] - acc_a[jj]);
+        o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
+      }
+      if (VERIFY && a.corr != nullptr && row0 == 0 && t - t0 < a.t_cap) {
+        float* cp = a.corr + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * kD + col0;
+#pragma unroll
+        for (int jj = 0; jj < G::VEC; jj += 4)
+          *reinterpret_cast<float4*>(cp + jj) = make_float4(u[jj], u[jj + 1], u[jj + 2], u[jj + 3]);
+      }
+      // S~ += (k / P_t) u^T
+      float2 u2[G::VEC / 2];
+      pairs_of<G::VEC>(u, u2);
+#pragma unroll
+      for (int i = 0; i < G::PASSES; ++i) {
+        const float4 c = s_coef[j][row0 + i * G::RPI];
+        const float2 ku = make_float2(c.z, c.w);
+#pragma unroll
+        for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = fma2(ku, u2[p], S.s[i][p]);
+      }
+      if (row0 == 0) store_out<G::VEC>(out + t * out_rs, o);
+    }
+    // restore the true state: S = P_end S~
+#pragma unroll
+    for (int i = 0; i < G::PASSES; ++i) {
+      const float2 pp = dup2(s_P[row0 + i * G::RPI]);
+#pragma unroll
+      for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = mul2(pp, S.s[i][p]);
+    }
+    tc0 += ne;
+  }
+  if (!VERIFY) strip_store<StateT, G>(sp, row0, col0, S);
+}
+
 namespace {
 
 template <typename StateT, int CW, int NW, bool VERIFY>
