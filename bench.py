@@ -250,7 +250,7 @@ def source_closure(name):
     seen, todo = [], [name]
     while todo:
         f = todo.pop()
-        if f in seen or not os.path.exists(os.path.join(CSRC, f)):
+        if not f or f in seen or not os.path.isfile(os.path.join(CSRC, f)):
             continue
         seen.append(f)
         with open(os.path.join(CSRC, f)) as fh:

@@ -1,0 +1,42 @@
+"""Host-side pieces of bench.py (CPU): the byte models and the validity check
+of the recorded ncu traffic against each kernel's sources."""
+
+import json
+import os
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_source_closure_follows_local_includes():
+    t1 = bench.source_closure("kda_t1.cu")
+    assert t1[0] != "" and "kda_t1.cu" in t1 and "kda_kernels.cuh" in t1 and "kda_device.cuh" in t1
+    assert "kda_stream.cu" not in t1 and "kda_api.cu" not in t1
+    st = bench.source_closure("kda_stream.cu")
+    assert {"kda_stream_common.cuh", "kda_async.cuh", "kda_kernels.cuh"} <= set(st)
+    assert bench.source_closure("") == [] and bench.source_closure("no_such_file.cu") == []
+
+
+def test_kernel_hashes_differ_per_translation_unit():
+    hashes = {f: bench.kernel_source_hash(f) for f in ("kda_t1.cu", "kda_stream.cu", "kda_spec.cu", "kda_fused.cu")}
+    assert len(set(hashes.values())) == 4
+    assert all(len(h) == 16 for h in hashes.values())
+
+
+def test_recorded_traffic_is_well_formed():
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    with open(path) as f:
+        rec = json.load(f)
+    for kind, e in rec["kernels"].items():
+        assert e["source"] in bench.SPLIT_SOURCE.values() or e["source"] == "kda_stream.cu", kind
+        assert e["dram_bytes_per_launch"] == e["dram_read_per_launch"] + e["dram_write_per_launch"]
+        assert "--clock-control none" in e["command"]
+        got = bench.ncu_traffic(kind)
+        assert got is None or got == e["dram_bytes_per_launch"]
+    assert bench.ncu_traffic("no_such_workload") is None
+
+
+def test_byte_models():
+    # fp32 state, bf16 activations: 2*64 KiB state + 4*256 B vectors + 2 B beta + 256 B out per unit
+    assert bench.bytes_t1(1, 0, 1, 4) - bench.bytes_t1(0, 0, 1, 4) == 2 * 128 * 128 * 4 + 4 * 256 + 2 + 256 + 4  # + the slot index
