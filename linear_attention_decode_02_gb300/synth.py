@@ -200,6 +200,58 @@ def spec_case(N, t_max, seed=0, H=16, lengths=None, pad_rows=0, null_count=0,
     return case
 
 
+def packed_fused_case(N, t_max, H=12, seed=0, lengths=None, cols=None, accepted=None, pad_rows=0,
+                      null_count=0, state_dtype=torch.float32, num_slots=None, make_state=True):
+    """Inputs of the packed fused speculative path (``kda_packed_fused_decode``).
+
+    Sequence n owns token rows qsl[n] .. qsl[n+1]-1 and the `cols` distinct
+    checkpoint slots state_indices[n, :]; it starts from column
+    num_accepted_tokens[n] - 1 (random in 1..cols unless `accepted` is given).
+    `null_count` sequences get a null start slot (0 or -1).  Token rows past
+    qsl[N] are `pad_rows` of graph padding.
+    """
+    gen = _gen(seed)
+    cols = cols or t_max
+    HD = H * D
+    if lengths is None:
+        lens = spec_lengths(gen, N, t_max)
+    else:
+        lens = torch.tensor(lengths, dtype=torch.int32)
+    qsl = torch.zeros(N + 1, dtype=torch.int32)
+    qsl[1:] = torch.cumsum(lens, 0)
+    R = int(qsl[-1]) + pad_rows
+    if num_slots is None:
+        num_slots = N * cols + 1
+    case = {
+        "x": _normal(gen, (R, 3 * HD), dtype=torch.bfloat16),
+        "conv_weight": _normal(gen, (3, 4, HD), std=0.5),
+        "raw_gate": _normal(gen, (R, H, D), dtype=torch.bfloat16),
+        "raw_beta": _normal(gen, (R, H), dtype=torch.bfloat16),
+        "A_log": _uniform(gen, (H,), -2.0, 0.0),
+        "dt_bias": _normal(gen, (HD,), std=0.1),
+        "query_start_loc": qsl,
+        "lengths": lens,
+        "t_max": int(t_max),
+    }
+    idx = distinct_slots(gen, N * cols, num_slots).reshape(N, cols)
+    if accepted is None:
+        acc = torch.randint(1, cols + 1, (N,), generator=gen, dtype=torch.int32)
+    else:
+        acc = torch.as_tensor(accepted, dtype=torch.int32).expand(N).clone()
+    if null_count > 0:
+        pick = torch.randperm(N, generator=gen)[:null_count]
+        for n in pick.tolist():
+            idx[n, int(acc[n]) - 1] = int(torch.randint(-1, 1, (1,), generator=gen))
+    case["state_indices"] = idx
+    case["num_accepted_tokens"] = acc
+    if make_state:
+        case["conv_state"] = conv_cache(gen, num_slots, 3 * HD)
+        case["state"] = state_pool(gen, num_slots, H, state_dtype)
+    case["output_gate"] = _normal(gen, (R, H, D), dtype=torch.bfloat16)
+    case["norm_weight"] = _normal(gen, (D,), std=0.1, mean=1.0)
+    return case
+
+
 def to_f64(t):
     """Exact upcast of a stored tensor to a float64 numpy array (bf16 is exact in f64)."""
     return t.detach().to("cpu").to(torch.float64).numpy()

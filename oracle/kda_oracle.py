@@ -31,7 +31,10 @@ Sources (web pages, cited by title and section):
   as an inactive padding row.
 * "feat(kda): add fused speculative decode kernel - #4809" (review thread on
   the T=1 row mapping): token rows past the last ``query_start_loc`` entry are
-  padding that write zero and touch no slot.
+  padding that write zero and touch no slot; the packed fused operation
+  updates conv and recurrent checkpoints from accepted-token metadata; its
+  bf16-state follow-up keeps the recurrence in float32 across the token loop
+  and rounds each per-token checkpoint on store.
 
 Readings where the pages are silent (each is a named constant or flag below):
 
@@ -49,6 +52,11 @@ Readings where the pages are silent (each is a named constant or flag below):
 * Output gate: RMSNorm over the 128 channels of a head (eps inside the square
   root), times ``norm_weight``, times ``sigmoid(output_gate)``.
 * Slot indices outside ``[1, num_slots)`` take the null path.
+* Packed fused checkpoints: ``state_indices`` is [N, C]; sequence n starts
+  from slot ``state_indices[n, num_accepted_tokens[n] - 1]`` and writes both
+  caches after its j-th token to slot ``state_indices[n, j]`` (j < C); a
+  non-live checkpoint slot is skipped; ``num_accepted_tokens`` outside 1..C
+  makes the sequence null.
 """
 
 from __future__ import annotations
@@ -318,6 +326,79 @@ def spec_decode(q, k, v, g, beta, cu_seqlens, state_indices, state,
                 S, out[t, h] = kda_step(S, q[t, h], k[t, h], v[t, h], g[t, h], rate[t, h], scale)
             state[s, h] = S
     return out, state
+
+
+def start_slot(row_slots, accepted):
+    """The slot a packed fused sequence starts from: the checkpoint of its
+    last accepted token, column accepted - 1 of its slot row."""
+    return int(row_slots[int(accepted) - 1])
+
+
+def packed_fused_decode(x, weight, conv_state, raw_gate, raw_beta, A_log, dt_bias,
+                        state_indices, query_start_loc, num_accepted_tokens, state,
+                        output_gate, norm_weight, lower_bound=PACKED_LOWER_BOUND,
+                        norm_eps=FUSED_NORM_EPS, scale=SCALE):
+    """Packed fused speculative decode with per-token checkpoints.
+
+    "feat(kda): add fused speculative decode kernel - #4809" (description and
+    the review thread on the T=1 row mapping) and its bf16-state follow-up:
+    the fused conv + KDA + gated-RMSNorm step of ``fused_decode`` run over the
+    T >= 1 token rows of each packed sequence, updating the conv and
+    recurrent caches from accepted-token metadata.
+
+    x: [R, 3*H*128] token rows; raw_gate, output_gate: [R, H, 128];
+    raw_beta: [R, H]; state_indices: [N, C] checkpoint slots per sequence;
+    query_start_loc: [N+1]; num_accepted_tokens: [N]; conv_state [M, 3*H*128, 3]
+    and state [M, H, 128, 128] are slot-indexed pools.
+
+    Sequence n owns token rows query_start_loc[n] .. query_start_loc[n+1]-1.
+    It starts from the caches of slot state_indices[n, a-1], a =
+    num_accepted_tokens[n] (the checkpoint of the last token accepted by the
+    previous step); after its j-th token (j < C) both caches are written to
+    slot state_indices[n, j] unless that slot is not live.  A sequence whose
+    start slot is not live, or whose a is outside 1..C, is null: zero output,
+    no cache written.  Rows outside [query_start_loc[0], query_start_loc[N])
+    are padding: zero output.  The state is carried in float64 across tokens
+    (the kernel's float32 registers); checkpoints are the carried values.
+    Returns (out [R, H, 128], new_state, new_conv_state).
+    """
+    x = np.asarray(x, np.float64)
+    R, C3 = x.shape
+    H = C3 // (3 * D)
+    HD = H * D
+    state = np.array(state, dtype=np.float64, copy=True)
+    conv_state = np.array(conv_state, dtype=np.float64, copy=True)
+    M = state.shape[0]
+    idx = np.asarray(state_indices).reshape(len(num_accepted_tokens), -1)
+    n_seq, cols = idx.shape
+    dt = np.asarray(dt_bias, np.float64).reshape(H, D)
+    out = np.zeros((R, H, D), dtype=np.float64)
+    for n in range(n_seq):
+        t0 = max(int(query_start_loc[n]), 0)
+        t1 = min(int(query_start_loc[n + 1]), R)
+        acc = int(num_accepted_tokens[n])
+        if t1 <= t0 or not 1 <= acc <= cols:
+            continue
+        s0 = start_slot(idx[n], acc)
+        if not _is_live(s0, M):
+            continue
+        S = state[s0].copy()
+        hist = conv_state[s0].copy()
+        for j, t in enumerate(range(t0, t1)):
+            a, hist = conv_update(x[t], weight, hist)
+            q = a[0:HD].reshape(H, D)
+            k = a[HD:2 * HD].reshape(H, D)
+            v = a[2 * HD:3 * HD].reshape(H, D)
+            g = gate(np.asarray(raw_gate[t], np.float64), dt, A_log, lower_bound)
+            beta = sigmoid(np.asarray(raw_beta[t], np.float64))
+            o = np.zeros((H, D))
+            for h in range(H):
+                S[h], o[h] = kda_step(S[h], q[h], k[h], v[h], g[h], beta[h], scale)
+            out[t] = gated_rmsnorm(o, np.asarray(output_gate[t], np.float64), norm_weight, norm_eps)
+            if j < cols and _is_live(int(idx[n, j]), M):
+                state[int(idx[n, j])] = S
+                conv_state[int(idx[n, j])] = hist
+    return out, state, conv_state
 
 
 def spec_verify(q, k, v, g, beta, cu_seqlens, state_indices, state, t_cap,

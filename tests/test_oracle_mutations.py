@@ -58,6 +58,8 @@ MUTATIONS = {
                        lambda x, eps=ko.L2_EPS: np.asarray(x, np.float64) /
                        (np.sqrt(np.sum(np.asarray(x, np.float64) ** 2, -1, keepdims=True)) + 1e-2)),
     "conv_taps_reversed": ("conv_weight_taps", lambda w: ORIG_CONV_TAPS(w)[:, ::-1]),
+    "start_from_column_zero": ("start_slot", lambda row, acc: int(row[0])),
+    "start_from_accepted_column": ("start_slot", lambda row, acc: int(row[min(int(acc), len(row) - 1)])),
     "rmsnorm_without_gate": ("gated_rmsnorm",
                              lambda o, g, w, eps=ko.FUSED_NORM_EPS: ORIG_RMS(o, np.full_like(g, 50.0), w, eps)),
 }

@@ -419,3 +419,116 @@ def test_verify_cache_capacity_and_null_rows():
     for s in range(M):
         if s not in live:
             assert not corr[s].any() and not kg[s].any()
+
+
+# --- packed fused speculative decode with per-token checkpoints -------------------
+
+def _pf(case):
+    c = _np(case)
+    return c, ko.packed_fused_decode(c["x"], c["conv_weight"], c["conv_state"], c["raw_gate"], c["raw_beta"],
+                                     c["A_log"], c["dt_bias"], c["state_indices"], c["query_start_loc"],
+                                     c["num_accepted_tokens"], c["state"], c["output_gate"], c["norm_weight"])
+
+
+def test_packed_fused_one_token_rows_are_fused_decode():
+    """query_start_loc = arange, one column, one accepted token: fused_decode on column 0."""
+    case = synth.packed_fused_case(5, 1, H=2, seed=21, lengths=[1] * 5, null_count=1)
+    c, (out, st, cs) = _pf(case)
+    o2, st2, cs2 = ko.fused_decode(c["x"], c["conv_weight"], c["conv_state"], c["raw_gate"], c["raw_beta"],
+                                   c["A_log"], c["dt_bias"], c["state_indices"][:, 0], c["state"],
+                                   c["output_gate"], c["norm_weight"])
+    np.testing.assert_allclose(out, o2, rtol=1e-14, atol=1e-16)
+    np.testing.assert_allclose(st, st2, rtol=1e-14, atol=1e-16)
+    np.testing.assert_array_equal(cs, cs2)
+
+
+def test_packed_fused_checkpoints_are_a_chain_of_fused_calls():
+    """Token j of a sequence and checkpoint j equal j+1 single-token fused
+    calls on a scratch slot holding the caches of the start slot."""
+    N, T, H = 4, 4, 2
+    case = synth.packed_fused_case(N, T, H=H, seed=22, lengths=[4, 2, 3, 1])
+    c, (out, st, cs) = _pf(case)
+    idx, acc, qsl = c["state_indices"], c["num_accepted_tokens"], c["query_start_loc"]
+    assert len(set(acc.tolist())) > 1  # several start columns exercised
+    for n in range(N):
+        s0 = int(idx[n, int(acc[n]) - 1])
+        pool = np.stack([np.zeros_like(c["state"][0]), c["state"][s0]])
+        conv = np.stack([np.zeros_like(c["conv_state"][0]), c["conv_state"][s0]])
+        for j, t in enumerate(range(int(qsl[n]), int(qsl[n + 1]))):
+            o1, pool, conv = ko.fused_decode(c["x"][t:t + 1], c["conv_weight"], conv, c["raw_gate"][t:t + 1],
+                                             c["raw_beta"][t:t + 1], c["A_log"], c["dt_bias"], np.array([1]),
+                                             pool, c["output_gate"][t:t + 1], c["norm_weight"])
+            np.testing.assert_allclose(out[t], o1[0], rtol=1e-13, atol=1e-15)
+            np.testing.assert_allclose(st[int(idx[n, j])], pool[1], rtol=1e-13, atol=1e-15)
+            np.testing.assert_array_equal(cs[int(idx[n, j])], conv[1])
+    # every slot no sequence checkpoints to is untouched
+    written = {int(idx[n, j]) for n in range(N) for j in range(int(c["lengths"][n]))}
+    for s in range(c["state"].shape[0]):
+        if s not in written:
+            np.testing.assert_array_equal(st[s], c["state"][s])
+            np.testing.assert_array_equal(cs[s], c["conv_state"][s])
+
+
+def test_packed_fused_conv_checkpoint_holds_the_last_three_raw_samples():
+    case = synth.packed_fused_case(1, 4, H=1, seed=23, lengths=[4], accepted=[2])
+    c, (_, _, cs) = _pf(case)
+    idx = c["state_indices"][0]
+    hist = np.concatenate([c["conv_state"][int(idx[1])], c["x"].T], axis=1)  # [C, 3 + 4] oldest first
+    for j in range(4):
+        np.testing.assert_array_equal(cs[int(idx[j])], hist[:, j + 1:j + 4])
+
+
+def _review_case(fx, seed):
+    n = len(fx["state_indices"])
+    lens = np.diff(fx["query_start_loc"]).tolist()
+    case = synth.packed_fused_case(n, 1, H=2, seed=seed, lengths=lens,
+                                   pad_rows=fx["num_token_rows"] - fx["query_start_loc"][-1], num_slots=8,
+                                   accepted=fx["num_accepted_tokens"])
+    case["state_indices"] = torch.tensor(fx["state_indices"], dtype=torch.int32)
+    return case
+
+
+def test_packed_fused_review_case_a_trailing_padding():
+    with open(os.path.join(GOLDEN, "packed_fused_review_cases.json")) as f:
+        fx = json.load(f)["case_a"]
+    c, (out, st, cs) = _pf(_review_case(fx, 24))
+    assert [s for s in range(8) if not np.array_equal(st[s], c["state"][s])] == fx["expected_mutated_slots"]
+    assert [s for s in range(8) if not np.array_equal(cs[s], c["conv_state"][s])] == fx["expected_mutated_slots"]
+    for r in fx["expected_zero_rows"]:
+        assert np.all(out[r] == 0.0)
+    assert np.all(np.abs(out[:2]).sum(-1) > 0)
+
+
+def test_packed_fused_review_case_b_empty_middle_sequence():
+    with open(os.path.join(GOLDEN, "packed_fused_review_cases.json")) as f:
+        fx = json.load(f)["case_b"]
+    c, (out, st, cs) = _pf(_review_case(fx, 25))
+    assert [s for s in range(8) if not np.array_equal(st[s], c["state"][s])] == fx["expected_mutated_slots"]
+    for r in fx["expected_zero_rows"]:
+        assert np.all(out[r] == 0.0)
+    # each live token row is the one-row fused decode on the slot the fixture names
+    for r, s in enumerate(fx["expected_row_slots"]):
+        o1, st1, _ = ko.fused_decode(c["x"][r:r + 1], c["conv_weight"], c["conv_state"], c["raw_gate"][r:r + 1],
+                                     c["raw_beta"][r:r + 1], c["A_log"], c["dt_bias"], np.array([s]), c["state"],
+                                     c["output_gate"][r:r + 1], c["norm_weight"])
+        np.testing.assert_allclose(out[r], o1[0], rtol=1e-14, atol=1e-16)
+        np.testing.assert_allclose(st[s], st1[s], rtol=1e-14, atol=1e-16)
+
+
+def test_packed_fused_null_start_and_null_checkpoint_columns():
+    case = synth.packed_fused_case(3, 3, H=1, seed=26, lengths=[3, 3, 2], accepted=[1, 2, 4])
+    case["state_indices"][0, 1] = -1  # checkpoint 1 of sequence 0 is not kept
+    case["state_indices"][1, 1] = 0   # sequence 1 starts from the null slot
+    c, (out, st, cs) = _pf(case)
+    idx, qsl = c["state_indices"], c["query_start_loc"]
+    # sequence 0: all three tokens decode, checkpoints 0 and 2 written, slot of column 1 is null
+    assert np.all(np.abs(out[0:3]).sum(-1) > 0)
+    assert not np.array_equal(st[int(idx[0, 0])], c["state"][int(idx[0, 0])])
+    assert not np.array_equal(st[int(idx[0, 2])], c["state"][int(idx[0, 2])])
+    # sequence 1 (null start) and sequence 2 (accepted 4 > 3 columns) are null
+    assert np.all(out[int(qsl[1]):] == 0.0)
+    for n in (1, 2):
+        for s in idx[n]:
+            if 0 < int(s) < c["state"].shape[0]:
+                np.testing.assert_array_equal(st[int(s)], c["state"][int(s)])
+                np.testing.assert_array_equal(cs[int(s)], c["conv_state"][int(s)])
