@@ -205,6 +205,42 @@ kda_status kda_spec_verify_decode(const kda_tensor* q, const kda_tensor* k, cons
                                   const kda_tensor* out, const kda_tensor* correction_cache,
                                   const kda_tensor* kg_cache, float scale, void* stream);
 
+/*
+ * kda_packed_fused_decode — packed fused speculative decode with per-token
+ * checkpoints ([P4] description, the review thread on the T=1 row mapping,
+ * and its bf16-state follow-up): the kda_fused_decode step (conv + SiLU, KDA,
+ * gated RMSNorm) run over the T >= 1 token rows of each of N packed
+ * sequences, one sequence after another's rows in x.
+ *
+ *   x, conv_weight, conv_state, raw_gate, raw_beta, A_log, dt_bias,
+ *   output_gate, norm_weight, has_lower_bound, lower_bound, norm_eps, out:
+ *               as kda_fused_decode, with R token rows in place of rows.
+ *   state_indices [N, C] int32, column stride 1: checkpoint slots of each
+ *               sequence (C >= 1).
+ *   query_start_loc [N+1] int32 contiguous, read on the device: sequence n
+ *               owns token rows qsl[n] .. qsl[n+1]-1 (clamped to [0, R)).
+ *   num_accepted_tokens [N] int32, read on the device: a_n.
+ *   state       [num_slots, H, 128, 128] float32 or bfloat16.
+ * Sequence n starts from the conv and recurrent caches of slot
+ * state_indices[n, a_n - 1] and, after its j-th token (j < C), writes both
+ * caches to slot state_indices[n, j]; a slot outside [1, num_slots) there is
+ * skipped.  The recurrence stays in float32 across the tokens; a bfloat16
+ * checkpoint is rounded once when stored.  A sequence whose start slot is
+ * null, or whose a_n is outside 1..C, writes zero output rows and no cache;
+ * empty sequences do nothing; token rows outside [qsl[0], qsl[N]) are
+ * padding with zero output.  Checkpoint slots must be distinct across the
+ * call (the start slot may be one of the sequence's own).
+ */
+kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight,
+                                   const kda_tensor* conv_state, const kda_tensor* raw_gate,
+                                   const kda_tensor* raw_beta, const kda_tensor* A_log,
+                                   const kda_tensor* dt_bias, const kda_tensor* state_indices,
+                                   const kda_tensor* query_start_loc,
+                                   const kda_tensor* num_accepted_tokens, const kda_tensor* state,
+                                   const kda_tensor* output_gate, const kda_tensor* norm_weight,
+                                   int32_t has_lower_bound, float lower_bound, float norm_eps,
+                                   const kda_tensor* out, void* stream);
+
 /* ---- host-only queries (no CUDA calls) ---------------------------------- */
 
 /* Operation ids for kda_plan_split. */

@@ -30,6 +30,7 @@ DEFAULT_SCALE = 1.0 / math.sqrt(128.0)
 
 # Every symbol include/kda.h declares.
 EXPORTS = ("kda_recurrent_decode", "kda_packed_decode", "kda_fused_decode", "kda_spec_decode",
+           "kda_packed_fused_decode",
            "kda_spec_verify_decode",
            "kda_plan_split", "kda_set_split_override", "kda_plan_schedule", "kda_set_schedule_override",
            "kda_device_error", "kda_selftest_wait_timeout", "kda_status_string", "kda_last_error_message",
@@ -57,6 +58,7 @@ def _declare(lib):
         "kda_recurrent_decode": [T, T, T, T, T, T, T, T, T, T, i32, f32, f32, vp],
         "kda_packed_decode": [T, T, T, T, T, T, T, T, vp],
         "kda_fused_decode": [T, T, T, T, T, T, T, T, T, T, T, i32, f32, f32, T, vp],
+        "kda_packed_fused_decode": [T, T, T, T, T, T, T, T, T, T, T, T, T, i32, f32, f32, T, vp],
         "kda_spec_decode": [T, T, T, T, T, i32, T, i32, T, T, T, f32, vp],
         "kda_spec_verify_decode": [T, T, T, T, T, i32, T, i32, T, T, T, T, T, f32, vp],
     }
@@ -170,6 +172,24 @@ def kda_fused_decode(x, conv_weight, conv_state, raw_gate, raw_beta, A_log, dt_b
                                   int(lower_bound is not None),
                                   float(lower_bound if lower_bound is not None else 0.0),
                                   float(norm_eps), _ref(out), _stream(x))
+    _check(lib, st)
+    return out
+
+
+def kda_packed_fused_decode(x, conv_weight, conv_state, raw_gate, raw_beta, A_log, dt_bias, state_indices,
+                            query_start_loc, num_accepted_tokens, state, output_gate, norm_weight,
+                            lower_bound=-5.0, norm_eps=1e-5, out=None):
+    """Packed fused speculative decode; writes per-token checkpoints of both caches, returns out [R, H, 128]."""
+    lib = library()
+    if out is None:
+        out = torch.empty((x.shape[0], state.shape[1], 128), dtype=torch.bfloat16, device=x.device)
+    with torch.cuda.device(x.device):
+        st = lib.kda_packed_fused_decode(_ref(x), _ref(conv_weight), _ref(conv_state), _ref(raw_gate),
+                                         _ref(raw_beta), _ref(A_log), _ref(dt_bias), _ref(state_indices),
+                                         _ref(query_start_loc), _ref(num_accepted_tokens), _ref(state),
+                                         _ref(output_gate), _ref(norm_weight), int(lower_bound is not None),
+                                         float(lower_bound if lower_bound is not None else 0.0),
+                                         float(norm_eps), _ref(out), _stream(x))
     _check(lib, st)
     return out
 

@@ -15,6 +15,7 @@
 
 #include "../../include/kda.h"
 #include "kda_launch.h"
+#include "kda_packed_fused.h"
 
 namespace {
 
@@ -572,6 +573,111 @@ kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, 
   a.scale = 0.08838834764831845f;  // 1/sqrt(128)
   if (sched == KDA_SCHED_STREAM) return check_launch(kda::launch_fused_stream(a, S.dtype, dev.sms, st));
   return check_launch(kda::launch_fused(a, S.dtype, st));
+}
+
+kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, const kda_tensor* conv_state,
+                                   const kda_tensor* raw_gate, const kda_tensor* raw_beta, const kda_tensor* A_log,
+                                   const kda_tensor* dt_bias, const kda_tensor* state_indices,
+                                   const kda_tensor* query_start_loc, const kda_tensor* num_accepted_tokens,
+                                   const kda_tensor* state, const kda_tensor* output_gate,
+                                   const kda_tensor* norm_weight, int32_t has_lower_bound, float lower_bound,
+                                   float norm_eps, const kda_tensor* out, void* stream) {
+  View X, W, C, G, Bt, A, DT, I, Q, AC, S, OG, NW, O;
+  KDA_TRY(ranked_view(x, "x", 2, -1, &X));
+  KDA_TRY(raw_view(conv_weight, "conv_weight", &W));
+  KDA_TRY(ranked_view(conv_state, "conv_state", 3, -1, &C));
+  KDA_TRY(ranked_view(raw_gate, "raw_gate", 3, 0, &G));
+  KDA_TRY(ranked_view(raw_beta, "raw_beta", 2, 0, &Bt));
+  KDA_TRY(raw_view(A_log, "A_log", &A));
+  KDA_TRY(raw_view(dt_bias, "dt_bias", &DT));
+  KDA_TRY(ranked_view(state_indices, "state_indices", 2, -1, &I));
+  KDA_TRY(raw_view(query_start_loc, "query_start_loc", &Q));
+  KDA_TRY(raw_view(num_accepted_tokens, "num_accepted_tokens", &AC));
+  KDA_TRY(raw_view(state, "state", &S));
+  KDA_TRY(ranked_view(output_gate, "output_gate", 3, 0, &OG));
+  KDA_TRY(raw_view(norm_weight, "norm_weight", &NW));
+  KDA_TRY(ranked_view(out, "out", 3, 0, &O));
+
+  KDA_CHECK(S.ndim == 4, KDA_ERR_INVALID_ARG, "state: expected rank 4");
+  const int64_t H = S.shape[1], HD = H * kD, R = X.shape[0];
+  KDA_CHECK(H >= 1, KDA_ERR_INVALID_ARG, "state: need at least one head");
+  KDA_TRY(need_state_layout(S, H));
+  KDA_TRY(need_dtype(X, KDA_BF16));
+  KDA_TRY(need_shape(X, 1, 3 * HD));
+  KDA_CHECK(X.stride[1] == 1, KDA_ERR_INVALID_ARG, "x: channel axis must have stride 1");
+  KDA_CHECK(R <= INT32_MAX, KDA_ERR_INVALID_ARG, "x: too many token rows");
+  KDA_TRY(need_dtype(W, KDA_F32));
+  KDA_CHECK(W.ndim == 3, KDA_ERR_INVALID_ARG, "conv_weight: expected rank 3");
+  KDA_TRY(need_shape(W, 0, 3));
+  KDA_TRY(need_shape(W, 1, 4));
+  KDA_TRY(need_shape(W, 2, HD));
+  KDA_TRY(need_contiguous(W));
+  KDA_TRY(need_dtype(C, KDA_BF16));
+  KDA_TRY(need_shape(C, 0, S.shape[0]));
+  KDA_TRY(need_shape(C, 1, 3 * HD));
+  KDA_TRY(need_shape(C, 2, 3));
+  KDA_CHECK(C.stride[1] == 1 && C.stride[2] == 3 * HD, KDA_ERR_INVALID_ARG,
+            "conv_state: strides must be [slot_stride, 1, 3*H*128]");
+  KDA_CHECK(C.shape[0] <= 1 || C.stride[0] >= 9 * HD, KDA_ERR_INVALID_ARG, "conv_state: slot stride overlaps slots");
+  KDA_TRY(need_dtype(G, KDA_BF16));
+  KDA_TRY(need_shape(G, 0, R));
+  KDA_TRY(need_shape(G, 1, H));
+  KDA_TRY(need_shape(G, 2, kD));
+  KDA_CHECK(G.stride[2] == 1, KDA_ERR_INVALID_ARG, "raw_gate: channel axis must have stride 1");
+  KDA_TRY(need_dtype(Bt, KDA_BF16));
+  KDA_TRY(need_shape(Bt, 0, R));
+  KDA_TRY(need_shape(Bt, 1, H));
+  KDA_TRY(need_f32_vector(A, H));
+  KDA_TRY(need_f32_vector(DT, HD));
+  KDA_TRY(need_dtype(I, KDA_I32));
+  const int64_t N = I.shape[0], cols = I.shape[1];
+  KDA_CHECK(cols >= 1 && cols <= INT32_MAX, KDA_ERR_INVALID_ARG, "state_indices: need at least one checkpoint column");
+  KDA_CHECK(N <= INT32_MAX - 1, KDA_ERR_INVALID_ARG, "state_indices: too many sequences");
+  KDA_CHECK(cols <= 1 || I.stride[1] == 1, KDA_ERR_INVALID_ARG, "state_indices: column stride must be 1");
+  KDA_TRY(need_indices(Q, N + 1));
+  KDA_TRY(need_indices(AC, N));
+  KDA_TRY(need_dtype(OG, KDA_BF16));
+  KDA_TRY(need_shape(OG, 0, R));
+  KDA_TRY(need_shape(OG, 1, H));
+  KDA_TRY(need_shape(OG, 2, kD));
+  KDA_TRY(need_vec_layout(OG));
+  KDA_TRY(need_f32_vector(NW, kD));
+  KDA_TRY(need_out(O));
+  KDA_TRY(need_shape(O, 0, R));
+  KDA_TRY(need_shape(O, 1, H));
+  KDA_TRY(need_shape(O, 2, kD));
+  KDA_TRY(check_gate(has_lower_bound, lower_bound));
+  KDA_CHECK(std::isfinite(norm_eps) && norm_eps >= 0.f, KDA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  KDA_TRY(no_alias(O, {&X, &W, &C, &G, &Bt, &A, &DT, &I, &Q, &AC, &S, &OG, &NW}));
+  KDA_TRY(no_alias(S, {&X, &W, &C, &G, &Bt, &A, &DT, &I, &Q, &AC, &OG, &NW}));
+  KDA_TRY(no_alias(C, {&X, &W, &G, &Bt, &A, &DT, &I, &Q, &AC, &OG, &NW}));
+  if (R == 0) return KDA_OK;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DeviceInfo dev;
+  KDA_TRY(current_device(st, &dev));
+  KDA_TRY(check_grid((N + 1) * H));
+
+  kda::PackedFusedArgs a{};
+  a.x = X.data; a.x_rs = X.stride[0];
+  a.conv_w = reinterpret_cast<const float*>(W.data);
+  a.conv_state = C.data; a.cs_slot_stride = C.stride[0]; a.cs_tap_stride = C.stride[2];
+  a.gate = G.data; a.g_rs = G.stride[0]; a.g_hs = G.stride[1];
+  a.beta = Bt.data; a.b_rs = Bt.stride[0]; a.b_hs = Bt.stride[1];
+  a.A_log = reinterpret_cast<const float*>(A.data);
+  a.dt_bias = reinterpret_cast<const float*>(DT.data);
+  a.qsl = reinterpret_cast<const int32_t*>(Q.data);
+  a.idx = reinterpret_cast<const int32_t*>(I.data); a.idx_rs = I.stride[0]; a.cols = (int32_t)cols;
+  a.accepted = reinterpret_cast<const int32_t*>(AC.data);
+  a.state = S.data; a.slot_stride = S.stride[0]; a.num_slots = (int32_t)S.shape[0];
+  a.out_gate = OG.data; a.og_rs = OG.stride[0]; a.og_hs = OG.stride[1];
+  a.norm_w = reinterpret_cast<const float*>(NW.data);
+  a.out = O.data; a.o_rs = H * kD;
+  a.N = (int32_t)N; a.R = (int32_t)R; a.H = (int32_t)H;
+  a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
+  a.lower_bound = lower_bound; a.norm_eps = norm_eps;
+  a.scale = 0.08838834764831845f;  // 1/sqrt(128)
+  return check_launch(kda::launch_packed_fused(a, S.dtype, st));
 }
 
 }  // extern "C"

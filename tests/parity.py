@@ -185,3 +185,59 @@ def oracle_verify(case, t_cap, rows=None, beta_is_logit=True, scale=ko.SCALE):
                                    t_cap, beta_is_logit=beta_is_logit, scale=scale)
     return ({tr: out[i] for i, tr in enumerate(tok)}, {s: corr[remap[s]] for s in slots},
             {s: kg[remap[s]] for s in slots})
+
+
+def oracle_packed_fused(case, seqs=None, lower_bound=-5.0, norm_eps=1e-5):
+    """Oracle over the sequences `seqs` on a compact pool of their slots:
+    ({token_row: out [H,128]}, {slot: S}, {slot: conv [C,3]}) for every slot
+    the oracle wrote."""
+    idx = case["state_indices"].numpy()
+    qsl = case["query_start_loc"].numpy()
+    acc = case["num_accepted_tokens"].numpy()
+    M = case["state"].shape[0]
+    N, cols = idx.shape
+    seqs = list(range(N)) if seqs is None else list(seqs)
+    slots = sorted({int(s) for n in seqs for s in idx[n] if 0 < int(s) < M})
+    remap = {s: i + 1 for i, s in enumerate(slots)}
+    sub_idx = np.array([[remap.get(int(s), -1) for s in idx[n]] for n in seqs]).reshape(len(seqs), cols)
+    R = case["x"].shape[0]
+    tok, sub_qsl = [], [0]
+    for n in seqs:
+        t0, t1 = max(int(qsl[n]), 0), min(int(qsl[n + 1]), R)
+        ts = list(range(t0, t1)) if t1 > t0 else []
+        tok += ts
+        sub_qsl.append(sub_qsl[-1] + len(ts))
+    t = torch.tensor(tok, dtype=torch.long)
+    sl = torch.tensor(slots, dtype=torch.long)
+    pool = _pool(case["state"], slots)
+    conv = np.zeros((len(slots) + 1,) + tuple(case["conv_state"].shape[1:]))
+    if slots:
+        conv[1:] = f64(case["conv_state"][sl])
+    out, st, cs = ko.packed_fused_decode(f64(case["x"][t]), f64(case["conv_weight"]), conv, f64(case["raw_gate"][t]),
+                                         f64(case["raw_beta"][t]), f64(case["A_log"]), f64(case["dt_bias"]),
+                                         sub_idx, np.array(sub_qsl), acc[seqs], pool, f64(case["output_gate"][t]),
+                                         f64(case["norm_weight"]), lower_bound=lower_bound, norm_eps=norm_eps)
+    written = {}
+    for s in slots:
+        i = remap[s]
+        if not (np.array_equal(st[i], pool[i]) and np.array_equal(cs[i], conv[i])):
+            written[s] = i
+    return ({tr: out[i] for i, tr in enumerate(tok)}, {s: st[i] for s, i in written.items()},
+            {s: cs[i] for s, i in written.items()})
+
+
+def packed_fused_written_slots(case):
+    """Slots the call must write: checkpoint columns j < len of live sequences."""
+    idx = case["state_indices"].numpy()
+    qsl = case["query_start_loc"].numpy()
+    acc = case["num_accepted_tokens"].numpy()
+    M, R = case["state"].shape[0], case["x"].shape[0]
+    N, cols = idx.shape
+    out = set()
+    for n in range(N):
+        t0, t1 = max(int(qsl[n]), 0), min(int(qsl[n + 1]), R)
+        a = int(acc[n])
+        if t1 <= t0 or not 1 <= a <= cols or not 0 < int(idx[n, a - 1]) < M:
+            continue
+        out |= {int(s) for s in idx[n, :min(t1 - t0, cols)] if 0 < int(s) < M}
+    return out

@@ -300,6 +300,61 @@ def test_spec_verify_contract(lib):
     assert _call_verify(lib, t, flat[: M * H * 4 * 128].view(M, H, 4, 128)) == ALIAS
 
 
+def _pf_args(R=5, N=3, C=2, H=2, M=9):
+    HD = H * 128
+    return dict(x=torch.zeros(R, 3 * HD, dtype=torch.bfloat16), conv_weight=torch.zeros(3, 4, HD),
+                conv_state=torch.zeros(M, 3, 3 * HD, dtype=torch.bfloat16).permute(0, 2, 1),
+                raw_gate=torch.zeros(R, H, 128, dtype=torch.bfloat16), raw_beta=torch.zeros(R, H, dtype=torch.bfloat16),
+                A_log=torch.zeros(H), dt_bias=torch.zeros(HD),
+                state_indices=torch.arange(1, N * C + 1, dtype=torch.int32).view(N, C),
+                query_start_loc=torch.tensor([0, 2, 4, 5], dtype=torch.int32)[: N + 1],
+                num_accepted_tokens=torch.ones(N, dtype=torch.int32), state=torch.zeros(M, H, 128, 128),
+                output_gate=torch.zeros(R, H, 128, dtype=torch.bfloat16), norm_weight=torch.ones(128),
+                out=torch.zeros(R, H, 128, dtype=torch.bfloat16))
+
+
+def _call_pf(lib, t, eps=1e-5):
+    d = {n: ctypes.byref(desc(v)) for n, v in t.items()}
+    return lib.kda_packed_fused_decode(d["x"], d["conv_weight"], d["conv_state"], d["raw_gate"], d["raw_beta"],
+                                       d["A_log"], d["dt_bias"], d["state_indices"], d["query_start_loc"],
+                                       d["num_accepted_tokens"], d["state"], d["output_gate"], d["norm_weight"],
+                                       1, -5.0, eps, d["out"], None)
+
+
+def test_packed_fused_contract(lib):
+    if NO_GPU:
+        assert _passes_validation(_call_pf(lib, _pf_args())), _msg(lib)
+    t = _pf_args()
+    t["state_indices"] = torch.ones(3, dtype=torch.int32)  # rank 1: needs [N, C]
+    assert _call_pf(lib, t) == INVALID
+    t = _pf_args()
+    t["state_indices"] = torch.ones(2, 3, dtype=torch.int32).t()  # column stride 2
+    assert _call_pf(lib, t) == INVALID
+    t = _pf_args()
+    t["query_start_loc"] = torch.zeros(3, dtype=torch.int32)  # needs N+1
+    assert _call_pf(lib, t) == INVALID
+    t = _pf_args()
+    t["num_accepted_tokens"] = torch.ones(2, dtype=torch.int32)
+    assert _call_pf(lib, t) == INVALID
+    t = _pf_args()
+    t["conv_state"] = torch.zeros(9, 3 * 256, 3, dtype=torch.bfloat16)  # tap-innermost layout
+    assert _call_pf(lib, t) == INVALID
+    t = _pf_args()
+    t["raw_gate"] = torch.zeros(4, 2, 128, dtype=torch.bfloat16)  # R mismatch
+    assert _call_pf(lib, t) == INVALID
+    assert _call_pf(lib, _pf_args(), eps=float("nan")) == INVALID
+    t = _pf_args()
+    t["out"] = t["output_gate"]
+    assert _call_pf(lib, t) == ALIAS
+    t = _pf_args()
+    t["x"] = torch.zeros(0, 768, dtype=torch.bfloat16)
+    for key in ("raw_gate", "output_gate", "out"):
+        t[key] = torch.zeros(0, 2, 128, dtype=torch.bfloat16)
+    t["raw_beta"] = torch.zeros(0, 2, dtype=torch.bfloat16)
+    t["query_start_loc"] = torch.zeros(4, dtype=torch.int32)
+    assert _call_pf(lib, t) == OK  # no token rows: nothing to launch
+
+
 def test_schedule_override_and_plan(lib):
     assert lib.kda_set_schedule_override(7) == INVALID
     assert lib.kda_set_schedule_override(2) == OK
