@@ -79,6 +79,22 @@ def bytes_spec(tokens_live, rows_live, rows, R, H, state_esize):
             + (rows + 1) * 4 + rows * 4)
 
 
+def bytes_packed_fused(seq_lens, cols, H, state_esize, R):
+    """Per live sequence and head: the state and conv cache read once, and
+    written once per checkpoint (min(len, cols) of them); per token: x, raw
+    gate, beta, output gate and out; padding rows: zero out; params once."""
+    conv = 3 * 3 * D * 2
+    unit = D * D * state_esize + conv
+    live_tokens = sum(seq_lens)
+    per_tok = 3 * D * 2 + D * 2 + 2 + D * 2 + D * 2
+    ckpts = sum(min(L, cols) for L in seq_lens if L > 0)
+    live = sum(1 for L in seq_lens if L > 0)
+    params = 3 * 4 * H * D * 4 + H * 4 + H * D * 4 + D * 4
+    n = len(seq_lens)
+    meta = (n + 1) * 4 + n * 4 + n * cols * 4
+    return (live + ckpts) * H * unit + live_tokens * H * per_tok + (R - live_tokens) * H * D * 2 + params + meta
+
+
 # ---- workloads ---------------------------------------------------------------------
 
 def _device_pool(num_slots, H, dtype, seed):
@@ -222,6 +238,43 @@ class Spec(Workload):
                                 self.t_max, out=self.out)
 
 
+class PackedFused(Workload):
+    """Packed fused speculative decode: N sequences of T tokens, one accepted
+    token (start column 0), a checkpoint after every token."""
+
+    def __init__(self, N=128, T=5, H=12, state_dtype=torch.float32, n_sets=2, seed=0):
+        cols = T
+        slots = n_sets * N * cols + 1
+        tag = "f32" if state_dtype == torch.float32 else "bf16"
+        self.name = f"packed_fused_h{H}_n{N}_t{T}_{tag}"
+        c = synth.packed_fused_case(N, T, H=H, seed=seed, lengths=[T] * N, accepted=1, num_slots=slots,
+                                    make_state=False)
+        self.d = {k: v.cuda() for k, v in c.items()
+                  if isinstance(v, torch.Tensor) and k not in ("state_indices", "lengths")}
+        self.d["state"] = _device_pool(slots, H, state_dtype, seed)
+        gen = torch.Generator(device="cuda").manual_seed(seed + 1)
+        phys = torch.empty(slots, 3, 3 * H * D, dtype=torch.float32, device="cuda").normal_(generator=gen)
+        self.d["conv_state"] = phys.to(torch.bfloat16).permute(0, 2, 1)
+        g = torch.Generator().manual_seed(seed + 7)
+        perm = (torch.randperm(slots - 1, generator=g) + 1).to(torch.int32)
+        self.sets = [perm[i * N * cols:(i + 1) * N * cols].view(N, cols).cuda() for i in range(n_sets)]
+        R = N * T
+        self.out = torch.empty(R, H, D, dtype=torch.bfloat16, device="cuda")
+        self.nbytes = bytes_packed_fused([T] * N, cols, H, 4 if state_dtype == torch.float32 else 2, R)
+        self.config = dict(workload="packed_fused_spec_checkpoints", H=H, sequences=N, tokens_per_sequence=T,
+                           num_accepted_tokens=1, checkpoint_columns=cols, num_slots=slots, state=
+                           "float32" if state_dtype == torch.float32 else "bfloat16", gate="lower_bound -5")
+        self.e2e_keys = ("x", "raw_gate", "raw_beta", "output_gate")
+        self.source = "kda_packed_fused.cu"
+
+    def call(self, idx):
+        d = self.d
+        binding.kda_packed_fused_decode(d["x"], d["conv_weight"], d["conv_state"], d["raw_gate"], d["raw_beta"],
+                                        d["A_log"], d["dt_bias"], idx, d["query_start_loc"],
+                                        d["num_accepted_tokens"], d["state"], d["output_gate"], d["norm_weight"],
+                                        out=self.out)
+
+
 def make_workload(args, seed):
     if args.workload == "recurrent":
         return Recurrent(B=args.batch or 512, H=args.heads or 32, slots=args.slots or 1024, seed=seed)
@@ -229,6 +282,9 @@ def make_workload(args, seed):
         return Packed(B=args.batch or 512, slots=args.slots or 2048, seed=seed)
     if args.workload == "fused":
         return Fused(H=args.heads or 32, rows=args.batch or 256, slots=args.slots or None, seed=seed)
+    if args.workload == "packed_fused":
+        return PackedFused(N=args.batch or 128, T=args.t_max or 5, H=args.heads or 12,
+                           state_dtype=torch.bfloat16 if args.bf16_state else torch.float32, seed=seed)
     return Spec(N=args.batch or 128, t_max=args.t_max or 6, H=args.heads or 16, slots=args.slots, seed=seed)
 
 
@@ -470,7 +526,7 @@ def e2e(wl, steps, warmup, barrier):
 
 
 def path_measurements(flush, peak):
-    """CUDA-graph timings of the four entry points over their configured sizes."""
+    """CUDA-graph timings of the decode entry points over their configured sizes."""
     res = {}
 
     def run(wl, n_sets):
@@ -489,6 +545,9 @@ def path_measurements(flush, peak):
         run(Fused(H=H, rows=rows, n_sets=n, seed=H + rows), n)
     for N, T in ((1, 6), (16, 6), (128, 2), (128, 4), (128, 6)):
         run(Spec(N=N, t_max=T, H=16, n_sets=2, seed=N + T), 2)
+    for H, N in ((12, 1), (12, 8), (12, 32), (12, 128), (24, 8), (24, 128)):
+        for dt in (torch.float32, torch.bfloat16):
+            run(PackedFused(N=N, T=5, H=H, state_dtype=dt, n_sets=2, seed=H + N), 2)
     torch.cuda.empty_cache()
     return res
 
@@ -550,7 +609,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=("recurrent", "packed", "fused", "spec"), default="recurrent")
+    ap.add_argument("--workload", choices=("recurrent", "packed", "fused", "spec", "packed_fused"),
+                    default="recurrent")
+    ap.add_argument("--bf16-state", action="store_true", help="packed_fused: bfloat16 state pool")
     ap.add_argument("--batch", type=int, default=0, help="rows (B / rows / N); 0 = the workload's default")
     ap.add_argument("--heads", type=int, default=0)
     ap.add_argument("--slots", type=int, default=0)

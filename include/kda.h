@@ -229,7 +229,10 @@ kda_status kda_spec_verify_decode(const kda_tensor* q, const kda_tensor* k, cons
  * null, or whose a_n is outside 1..C, writes zero output rows and no cache;
  * empty sequences do nothing; token rows outside [qsl[0], qsl[N]) are
  * padding with zero output.  Checkpoint slots must be distinct across the
- * call (the start slot may be one of the sequence's own).
+ * call (the start slot may be one of the sequence's own).  The rows of x,
+ * raw_gate and output_gate are copied to shared memory in 16-byte pieces:
+ * their base addresses and outer strides must be multiples of 16 bytes
+ * (KDA_ERR_UNSUPPORTED otherwise).
  */
 kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight,
                                    const kda_tensor* conv_state, const kda_tensor* raw_gate,
@@ -244,14 +247,22 @@ kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_w
 /* ---- host-only queries (no CUDA calls) ---------------------------------- */
 
 /* Operation ids for kda_plan_split. */
-typedef enum kda_op { KDA_OP_RECURRENT = 0, KDA_OP_PACKED = 1, KDA_OP_FUSED = 2, KDA_OP_SPEC = 3 } kda_op;
+typedef enum kda_op {
+  KDA_OP_RECURRENT = 0,
+  KDA_OP_PACKED = 1,
+  KDA_OP_FUSED = 2,
+  KDA_OP_SPEC = 3,
+  KDA_OP_PACKED_FUSED = 4
+} kda_op;
 
 /*
  * Value-column split the dispatcher picks for `units` = rows * heads on a
  * device with `sm_count` SMs (state_dtype: KDA_F32 / KDA_BF16; t_max: tokens
  * per row, 1 for T=1).  Each CTA then owns 128/split value columns of one
  * unit.  Returns the split (1, 2, 4, 8 or 16), or 0 on invalid arguments.
- * Honors kda_set_split_override.
+ * Honors kda_set_split_override.  For KDA_OP_PACKED_FUSED (units =
+ * sequences * heads) the split is the size of the thread-block cluster that
+ * shares a unit (1, 2, 4 or 8; a forced 16 runs as 8).
  */
 int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max,
                        int32_t sm_count);

@@ -268,7 +268,7 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
 //  - speculative rows: the split kernel.
 int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)t_max;
-  if (op == KDA_OP_SPEC) return KDA_SCHED_SPLIT;
+  if (op == KDA_OP_SPEC || op == KDA_OP_PACKED_FUSED) return KDA_SCHED_SPLIT;
   const int forced = g_schedule_override.load();
   if (forced != KDA_SCHED_AUTO) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
@@ -285,17 +285,25 @@ bool rows_aligned16(const View& v) {
   return true;
 }
 
+// Packed fused speculative decode: CTAs per (sequence, head) cluster.
+// Measured on GB300 (H=12/24, T=5, CUDA-graph replays after an L2 flush):
+// one CTA per unit is best from 8 sequences of 12 heads up; two tie or win
+// slightly below a quarter of the SM count in units; 4 and 8 lose (their
+// CTAs of 2 warps stretch the conv and coefficient phases).
+int plan_cluster(int64_t units, int sms) { return 4 * units <= sms ? 2 : 1; }
+
 int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)state_dtype;
   (void)t_max;
   const int forced = g_split_override.load();
   if (op == KDA_OP_FUSED) return 1;
-  if (forced != 0) return forced;
+  if (forced != 0) return op == KDA_OP_PACKED_FUSED ? (forced > 8 ? 8 : forced) : forced;
   // Measured on GB300 for the split kernel: speculative rows (T tokens of
   // work per state block) 2 value slabs per unit at every size; T=1 with
   // the units at five or more per SM 4 slabs, fewer than half the SM count
   // 16 slabs, 8 in between.
   if (op == KDA_OP_SPEC) return 2;
+  if (op == KDA_OP_PACKED_FUSED) return plan_cluster(units, sms);
   if (units >= 5LL * sms) return 4;
   return 2 * units <= sms ? 16 : 8;
 }
@@ -648,6 +656,8 @@ kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_w
   KDA_TRY(need_shape(O, 2, kD));
   KDA_TRY(check_gate(has_lower_bound, lower_bound));
   KDA_CHECK(std::isfinite(norm_eps) && norm_eps >= 0.f, KDA_ERR_INVALID_ARG, "norm_eps must be finite and >= 0");
+  KDA_CHECK(rows_aligned16(X) && rows_aligned16(G) && rows_aligned16(OG), KDA_ERR_UNSUPPORTED,
+            "x, raw_gate and output_gate rows must start on 16-byte boundaries (base and outer strides)");
   KDA_TRY(no_alias(O, {&X, &W, &C, &G, &Bt, &A, &DT, &I, &Q, &AC, &S, &OG, &NW}));
   KDA_TRY(no_alias(S, {&X, &W, &C, &G, &Bt, &A, &DT, &I, &Q, &AC, &OG, &NW}));
   KDA_TRY(no_alias(C, {&X, &W, &G, &Bt, &A, &DT, &I, &Q, &AC, &OG, &NW}));
@@ -656,7 +666,8 @@ kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_w
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DeviceInfo dev;
   KDA_TRY(current_device(st, &dev));
-  KDA_TRY(check_grid((N + 1) * H));
+  const int cluster = plan_split(KDA_OP_PACKED_FUSED, N * H, S.dtype, 1, dev.sms);
+  KDA_TRY(check_grid((N + 1) * H * cluster));
 
   kda::PackedFusedArgs a{};
   a.x = X.data; a.x_rs = X.stride[0];
@@ -677,7 +688,7 @@ kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_w
   a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
   a.lower_bound = lower_bound; a.norm_eps = norm_eps;
   a.scale = 0.08838834764831845f;  // 1/sqrt(128)
-  return check_launch(kda::launch_packed_fused(a, S.dtype, st));
+  return check_launch(kda::launch_packed_fused(a, S.dtype, cluster, st));
 }
 
 }  // extern "C"
@@ -810,13 +821,13 @@ kda_status kda_spec_verify_decode(const kda_tensor* q, const kda_tensor* k, cons
 }
 
 int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max, int32_t sm_count) {
-  if (op < KDA_OP_RECURRENT || op > KDA_OP_SPEC || units < 0 || sm_count < 1 || t_max < 1) return 0;
+  if (op < KDA_OP_RECURRENT || op > KDA_OP_PACKED_FUSED || units < 0 || sm_count < 1 || t_max < 1) return 0;
   if (state_dtype != KDA_F32 && state_dtype != KDA_BF16) return 0;
   return plan_split(op, units, state_dtype, t_max, sm_count);
 }
 
 int32_t kda_plan_schedule(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max, int32_t sm_count) {
-  if (op < KDA_OP_RECURRENT || op > KDA_OP_SPEC || units < 0 || sm_count < 1 || t_max < 1) return 0;
+  if (op < KDA_OP_RECURRENT || op > KDA_OP_PACKED_FUSED || units < 0 || sm_count < 1 || t_max < 1) return 0;
   if (state_dtype != KDA_F32 && state_dtype != KDA_BF16) return 0;
   return plan_schedule(op, units, state_dtype, t_max, sm_count);
 }

@@ -1,48 +1,105 @@
 // Packed fused speculative decode (conv + SiLU + KDA + gated RMSNorm over
 // T >= 1 token rows per sequence) with per-token checkpoints of both caches.
+#include <cooperative_groups.h>
+
 #include "kda_kernels.cuh"
 #include "kda_packed_fused.h"
 
+namespace cg = cooperative_groups;
+
 namespace kda {
 
+namespace {
+
+// 16-byte global -> shared copy through L2 (cp.async.cg); completes at the
+// next cp_async_wait_all of the issuing thread.
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+               "l"(src)
+               : "memory");
+}
+// 4-byte global -> shared copy (cp.async.ca), same completion rule.
+__device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+}  // namespace
+
 // =====================================================================================
-// One CTA of 8 warps per (sequence, head); warp w owns value columns
-// 16w..16w+15 over all 128 key rows.  The state is loaded once from the
-// start slot (the checkpoint of the last accepted token) and carried in
-// float32 registers across the sequence's tokens; after each token it is
-// stored to that token's checkpoint slot (rounded once if bf16), so a call
-// moves one state read plus one state write per token.
+// One cluster of CL CTAs per (sequence, head); CTA `rank` owns the value
+// columns [rank*W, rank*W + W), W = CW*NW, warp w a strip of CW of them over
+// all 128 key rows.  The state slab is loaded once from the start slot (the
+// checkpoint of the last accepted token) and carried in float32 registers
+// across the sequence's tokens; after each token it is stored to that
+// token's checkpoint slot (rounded once if bf16), so a call moves one state
+// read plus one state write per token.
+//
+// The prologue keeps dependent memory round trips to three: the parameters
+// (conv taps, dt_bias, norm weight) are copied to shared memory
+// asynchronously at entry, alongside the metadata loads (token range,
+// accepted count, the first chunk's checkpoint slots); the chunk's
+// activation rows (the q and k sections of x and this CTA's slab of its v
+// section, the raw gate, this slab of the output gate: 16-byte pieces) are
+// staged as soon as the token range is known, alongside the start-slot
+// lookup; then the state slab and the conv history are loaded.
 //
 // Tokens go in chunks of up to TC:
-//  A. conv + SiLU of the chunk's tokens for this head's 384 channels (each
-//     thread carries the raw history of its channels in registers and writes
-//     the per-token conv checkpoints), decays and betas;
-//  B. warp j normalises q, k of token j and writes its per-row coefficients;
+//  A. conv + SiLU of the chunk's tokens for the CTA's 256 + W channels (each
+//     thread carries the raw history of its channels; a CTA writes the conv
+//     checkpoints of its slab of each section, so every channel is written
+//     once per cluster);
+//  B. the warps normalise q, k of the chunk's tokens, form the decays and
+//     write the per-row coefficients (all 128 key rows, in every CTA);
 //  C. every warp runs the chunk's tokens on its strip with no CTA barrier:
 //     reduction, update, checkpoint store, raw output and its sum of squares;
-//  D. warp j applies the gated RMSNorm to token j and writes the output row.
+//  D. the RMSNorm sum of squares is combined over the cluster through
+//     distributed shared memory, and each CTA writes its slab of the gated
+//     outputs.
 // Grid slice n == N zeroes the padding token rows outside [qsl[0], qsl[N]).
 // =====================================================================================
-template <typename StateT>
-__global__ void __launch_bounds__(256, 2) kda_packed_fused_kernel(const PackedFusedArgs a) {
-  constexpr int CW = 16, NW = 8, NT = NW * 32, TC = 8, NCH = 3 * kD;
+template <typename StateT, int CW, int NW>
+__global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fused_kernel(const PackedFusedArgs a) {
+  constexpr int NT = NW * 32, TC = 8;
+  constexpr int W = CW * NW;       // value columns of this CTA
+  constexpr int CL = kD / W;       // CTAs per (sequence, head)
+  constexpr int NCH = 2 * kD + W;  // conv channels: all of q and k, this slab of v
+  constexpr int PT = 48 + W / 4;   // 16-byte staging pieces per token
   using G = Strip<StateT, CW>;
-  static_assert(CW * NW == kD, "one CTA covers all value columns");
-  static_assert(TC <= NW, "phases B and D give each token of a chunk one warp");
-  __shared__ __align__(16) float s_act[TC][NCH];  // SiLU(conv): q | k | v channels of this head
-  __shared__ __align__(16) float s_d[TC][kD];     // decay exp(g)
-  __shared__ float4 s_coef[TC][kD];               // (d k_hat, d q_hat, d, k_hat) per key row
-  __shared__ float2 s_tok[TC];                    // (beta, q_hat . k_hat)
-  __shared__ int s_slot[TC];                      // checkpoint slot, 0 = none
-  __shared__ __align__(16) float s_o[TC][kD];     // raw outputs
-  __shared__ float s_ss[TC][NW];                  // per-warp sums of squares
+  static_assert(CL * W == kD && (CL == 1 || CL == 2 || CL == 4 || CL == 8), "slabs must tile the 128 columns");
+  static_assert(W % 8 == 0, "slabs are staged in 16-byte pieces");
+  // The staged conv input (read in phase A) and the raw outputs (written in
+  // phase C) share one buffer.
+  constexpr int XO_BYTES = TC * NCH * 2 > TC * W * 4 ? TC * NCH * 2 : TC * W * 4;
+  __shared__ __align__(16) unsigned char s_xo[XO_BYTES];
+  auto s_x = reinterpret_cast<__nv_bfloat16 (*)[NCH]>(s_xo);  // staged conv input: q | k | v slab
+  auto s_o = reinterpret_cast<float (*)[W]>(s_xo);            // raw outputs (slab)
+  __shared__ float s_w[4][NCH];                         // conv taps of the CTA's channels
+  __shared__ __align__(16) float s_dt[kD];              // dt_bias of this head
+  __shared__ __align__(16) float s_nw[W];               // norm weight (slab)
+  __shared__ __align__(16) __nv_bfloat16 s_gr[TC][kD];  // staged raw gates
+  __shared__ __align__(16) __nv_bfloat16 s_og[TC][W];   // staged output-gate logits (slab)
+  __shared__ __align__(16) float s_act[TC][NCH];        // SiLU(conv)
+  __shared__ float4 s_coef[TC][kD];                     // (d k_hat, d q_hat, d, k_hat) per key row
+  __shared__ float2 s_tok[TC];                          // (beta, q_hat . k_hat)
+  __shared__ int s_slot[TC];                            // checkpoint slot, 0 = none
+  __shared__ float s_ss[TC][NW];                        // per-warp sums of squares
+  __shared__ float s_part[TC];                          // this CTA's sum of squares per token
+  __shared__ __nv_bfloat16 s_hist[3][NCH];              // raw conv history, oldest first (thread-owned)
 
-  const int h = blockIdx.x % a.H;
-  const int n = blockIdx.x / a.H;
+  const int rank = CL == 1 ? 0 : (int)(blockIdx.x % CL);
+  const int unit = blockIdx.x / CL;
+  const int h = unit % a.H;
+  const int n = unit / a.H;
+  const int slab0 = rank * W;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int col0 = warp * CW + (lane % G::LPR) * G::VEC;
+  const int lcol = warp * CW + (lane % G::LPR) * G::VEC;  // column within the slab
+  const int col0 = slab0 + lcol;
   const int row0 = lane / G::LPR;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD;
 
@@ -54,14 +111,69 @@ __global__ void __launch_bounds__(256, 2) kda_packed_fused_kernel(const PackedFu
     return;
   }
 
+  const int HD = a.H * kD;
+  // Section and channel-within-section of local conv channel lc.
+  auto sec_of = [](int lc) { return lc < kD ? 0 : (lc < 2 * kD ? 1 : 2); };
+  auto cis_of = [slab0](int lc) { return lc < 2 * kD ? (lc & (kD - 1)) : slab0 + lc - 2 * kD; };
+
+  // Parameters first: they depend on nothing, so their copies overlap the
+  // metadata loads below.
+  for (int lc = tid; lc < NCH; lc += NT) {
+    const float* w = a.conv_w + (int64_t)sec_of(lc) * 4 * HD + h * kD + cis_of(lc);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) cp_async4(&s_w[p][lc], w + (int64_t)p * HD);
+  }
+  for (int i = tid; i < 32 + W / 4; i += NT) {
+    if (i < 32) cp_async16(&s_dt[4 * i], a.dt_bias + h * kD + 4 * i);
+    else cp_async16(&s_nw[4 * (i - 32)], a.norm_w + slab0 + 4 * (i - 32));
+  }
+  cp_async_commit();
+  const float A = expf(__ldg(a.A_log + h));
+
+  const int32_t* row_slots = a.idx + (int64_t)n * a.idx_rs;
   const int t0 = max(__ldg(a.qsl + n), 0);
   const int t1 = min(__ldg(a.qsl + n + 1), a.R);
-  if (t1 <= t0) return;  // empty sequence: nothing written
   const int acc = __ldg(a.accepted + n);
-  const int32_t* row_slots = a.idx + (int64_t)n * a.idx_rs;
-  const int s0 = (acc >= 1 && acc <= a.cols) ? __ldg(row_slots + acc - 1) : 0;
+  int slot = (tid < TC && tid < a.cols) ? __ldg(row_slots + tid) : 0;  // first chunk's checkpoints
+  if (t1 <= t0) {  // empty sequence: nothing written
+    cp_async_wait_all();
+    return;
+  }
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(a.x);
+  const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.gate);
+  const __nv_bfloat16* ogb = static_cast<const __nv_bfloat16*>(a.out_gate);
+
+  auto stage = [&](int tc0, int nt) {
+    for (int i = tid; i < nt * PT; i += NT) {
+      const int j = i / PT, c = i % PT;
+      const int64_t t = tc0 + j;
+      const __nv_bfloat16* xr = xb + t * a.x_rs + h * kD;
+      if (c < 32) {  // q, k sections: all 128 channels
+        const int sec = c >> 4, part = c & 15;
+        cp_async16(&s_x[j][sec * kD + part * 8], xr + (int64_t)sec * HD + part * 8);
+      } else if (c < 32 + W / 8) {  // v section: this slab
+        const int part = c - 32;
+        cp_async16(&s_x[j][2 * kD + part * 8], xr + 2 * (int64_t)HD + slab0 + part * 8);
+      } else if (c < 48 + W / 8) {
+        const int part = c - 32 - W / 8;
+        cp_async16(&s_gr[j][part * 8], gb + t * a.g_rs + (int64_t)h * a.g_hs + part * 8);
+      } else {
+        const int part = c - 48 - W / 8;
+        cp_async16(&s_og[j][part * 8], ogb + t * a.og_rs + (int64_t)h * a.og_hs + slab0 + part * 8);
+      }
+    }
+    cp_async_commit();
+  };
+
+  stage(t0, min(TC, t1 - t0));
+  float braw = tid < min(TC, t1 - t0) ? __bfloat162float(static_cast<const __nv_bfloat16*>(a.beta)[
+                                            (int64_t)(t0 + tid) * a.b_rs + (int64_t)h * a.b_hs])
+                                      : 0.f;
+  const bool live_acc = acc >= 1 && acc <= a.cols;
+  const int s0 = live_acc ? __ldg(row_slots + acc - 1) : 0;
   if (s0 <= 0 || s0 >= a.num_slots) {  // null sequence: zero its rows, touch no cache
     for (int t = t0 + row0; t < t1; t += G::RPI) store_out_zero<G::VEC>(out + t * a.o_rs + col0);
+    cp_async_wait_all();
     return;
   }
 
@@ -69,83 +181,75 @@ __global__ void __launch_bounds__(256, 2) kda_packed_fused_kernel(const PackedFu
   FltRegs<G> S;
   strip_load<StateT, G>(static_cast<const StateT*>(a.state) + (int64_t)s0 * a.slot_stride + head_off, row0, col0, S);
 
-  // Raw conv history (oldest first) of the thread's channels lc = tid, tid + 256.
-  const int HD = a.H * kD;
-  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(a.x);
   __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
-  constexpr int NC = (NCH + NT - 1) / NT;
-  __nv_bfloat16 hist[NC][3];
-  int chan[NC];
+  for (int lc = tid; lc < NCH; lc += NT) {
+    const __nv_bfloat16* cp = cs + (int64_t)s0 * a.cs_slot_stride + sec_of(lc) * HD + h * kD + cis_of(lc);
 #pragma unroll
-  for (int c = 0; c < NC; ++c) {
-    const int lc = tid + c * NT;
-    chan[c] = lc < NCH ? (lc >> 7) * HD + h * kD + (lc & (kD - 1)) : 0;
-    if (lc < NCH) {
-      const __nv_bfloat16* cp = cs + (int64_t)s0 * a.cs_slot_stride + chan[c];
-#pragma unroll
-      for (int p = 0; p < 3; ++p) hist[c][p] = cp[p * a.cs_tap_stride];
-    }
+    for (int p = 0; p < 3; ++p) s_hist[p][lc] = cp[p * a.cs_tap_stride];
   }
-  const float A = expf(__ldg(a.A_log + h));
-  const float dtb = tid < kD ? __ldg(a.dt_bias + h * kD + tid) : 0.f;
-  const float4 nw = __ldg(reinterpret_cast<const float4*>(a.norm_w) + lane);
 
   for (int tc0 = t0; tc0 < t1; tc0 += TC) {
     const int nt = min(TC, t1 - tc0);
     const int p0 = tc0 - t0;  // position of the chunk's first token in its sequence
-    if (tc0 != t0) __syncthreads();  // previous chunk's epilogue done with the shared arrays
-
-    // ---- A: conv + SiLU, conv checkpoints, decays, betas, checkpoint slots
-#pragma unroll
-    for (int c = 0; c < NC; ++c) {
-      const int lc = tid + c * NT;
-      if (lc >= NCH) continue;
-      const int sec = lc >> 7;
-      const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + (lc & (kD - 1));
-      const float w0 = __ldg(w), w1 = __ldg(w + HD), w2 = __ldg(w + 2 * HD), w3 = __ldg(w + 3 * HD);
-      for (int j = 0; j < nt; ++j) {
-        const int t = tc0 + j;
-        const __nv_bfloat16 xn = xb[(int64_t)t * a.x_rs + chan[c]];
-        float y = w0 * __bfloat162float(hist[c][0]);
-        y = fmaf(w1, __bfloat162float(hist[c][1]), y);
-        y = fmaf(w2, __bfloat162float(hist[c][2]), y);
-        y = fmaf(w3, __bfloat162float(xn), y);
-        s_act[j][lc] = y * sigmoidf_(y);
-        hist[c][0] = hist[c][1];
-        hist[c][1] = hist[c][2];
-        hist[c][2] = xn;
-        if (p0 + j < a.cols) {
-          const int sl = __ldg(row_slots + p0 + j);
-          if (sl > 0 && sl < a.num_slots) {
-            __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + chan[c];
-#pragma unroll
-            for (int p = 0; p < 3; ++p) cp[p * a.cs_tap_stride] = hist[c][p];
-          }
-        }
+    if (tc0 != t0) {
+      __syncthreads();  // previous chunk's epilogue done with the shared arrays
+      stage(tc0, nt);
+      if (tid < nt) {
+        braw = __bfloat162float(
+            static_cast<const __nv_bfloat16*>(a.beta)[(int64_t)(tc0 + tid) * a.b_rs + (int64_t)h * a.b_hs]);
+        slot = p0 + tid < a.cols ? __ldg(row_slots + p0 + tid) : 0;
       }
     }
-    if (tid < kD) {
-      const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.gate) + (int64_t)h * a.g_hs + tid;
-      for (int j = 0; j < nt; ++j)
-        s_d[j][tid] = expf(log_decay(__bfloat162float(gp[(int64_t)(tc0 + j) * a.g_rs]) + dtb, A, a.gate_mode,
-                                     a.lower_bound));
-    }
+    cp_async_wait_all();
     if (tid < nt) {
-      const float braw = __bfloat162float(
-          static_cast<const __nv_bfloat16*>(a.beta)[(int64_t)(tc0 + tid) * a.b_rs + (int64_t)h * a.b_hs]);
       s_tok[tid].x = sigmoidf_(braw);
-      int sl = p0 + tid < a.cols ? __ldg(row_slots + p0 + tid) : 0;
-      s_slot[tid] = (sl > 0 && sl < a.num_slots) ? sl : 0;
+      s_slot[tid] = (slot > 0 && slot < a.num_slots) ? slot : 0;
     }
     __syncthreads();
 
-    // ---- B: per-token coefficients, one warp per token
-    if (warp < nt) {
-      const float4 q = *reinterpret_cast<const float4*>(&s_act[warp][4 * lane]);
-      const float4 k = *reinterpret_cast<const float4*>(&s_act[warp][kD + 4 * lane]);
-      const float4 d = *reinterpret_cast<const float4*>(&s_d[warp][4 * lane]);
-      const float qk = token_coefficients(q, k, d, lane, s_coef[warp]);
-      if (lane == 0) s_tok[warp].y = qk;
+    // ---- A: conv + SiLU and this CTA's share of the conv checkpoints
+    for (int lc = tid; lc < NCH; lc += NT) {
+      const int sec = sec_of(lc), cis = cis_of(lc);
+      const int64_t ch = (int64_t)sec * HD + h * kD + cis;
+      const bool owner = cis >= slab0 && cis < slab0 + W;
+      const float w0 = s_w[0][lc], w1 = s_w[1][lc], w2 = s_w[2][lc], w3 = s_w[3][lc];
+      __nv_bfloat16 h0 = s_hist[0][lc], h1 = s_hist[1][lc], h2 = s_hist[2][lc];
+      for (int j = 0; j < nt; ++j) {
+        const __nv_bfloat16 xn = s_x[j][lc];
+        float y = w0 * __bfloat162float(h0);
+        y = fmaf(w1, __bfloat162float(h1), y);
+        y = fmaf(w2, __bfloat162float(h2), y);
+        y = fmaf(w3, __bfloat162float(xn), y);
+        s_act[j][lc] = y * sigmoidf_(y);
+        h0 = h1;
+        h1 = h2;
+        h2 = xn;
+        const int sl = s_slot[j];
+        if (owner && sl != 0) {
+          __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + ch;
+          cp[0] = h0;
+          cp[a.cs_tap_stride] = h1;
+          cp[2 * a.cs_tap_stride] = h2;
+        }
+      }
+      s_hist[0][lc] = h0;
+      s_hist[1][lc] = h1;
+      s_hist[2][lc] = h2;
+    }
+    __syncthreads();
+
+    // ---- B: per-token decays and coefficients
+    for (int j = warp; j < nt; j += NW) {
+      const float4 dtb = *reinterpret_cast<const float4*>(&s_dt[4 * lane]);
+      const float4 q = *reinterpret_cast<const float4*>(&s_act[j][4 * lane]);
+      const float4 k = *reinterpret_cast<const float4*>(&s_act[j][kD + 4 * lane]);
+      const uint2 gr = *reinterpret_cast<const uint2*>(&s_gr[j][4 * lane]);
+      const float4 d = make_float4(expf(log_decay(bf_lo(gr.x) + dtb.x, A, a.gate_mode, a.lower_bound)),
+                                   expf(log_decay(bf_hi(gr.x) + dtb.y, A, a.gate_mode, a.lower_bound)),
+                                   expf(log_decay(bf_lo(gr.y) + dtb.z, A, a.gate_mode, a.lower_bound)),
+                                   expf(log_decay(bf_hi(gr.y) + dtb.w, A, a.gate_mode, a.lower_bound)));
+      const float qk = token_coefficients(q, k, d, lane, s_coef[j]);
+      if (lane == 0) s_tok[j].y = qk;
     }
     __syncthreads();
 
@@ -158,7 +262,7 @@ __global__ void __launch_bounds__(256, 2) kda_packed_fused_kernel(const PackedFu
       float ss = 0.f;
 #pragma unroll
       for (int jj = 0; jj < G::VEC; ++jj) {
-        u[jj] = tk.x * (s_act[j][2 * kD + col0 + jj] - acc_a[jj]);
+        u[jj] = tk.x * (s_act[j][2 * kD + lcol + jj] - acc_a[jj]);
         o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
         ss = fmaf(o[jj], o[jj], ss);
       }
@@ -168,37 +272,79 @@ __global__ void __launch_bounds__(256, 2) kda_packed_fused_kernel(const PackedFu
         strip_store<StateT, G>(static_cast<StateT*>(a.state) + (int64_t)sl * a.slot_stride + head_off, row0, col0, S);
       if (row0 == 0) {
 #pragma unroll
-        for (int jj = 0; jj < G::VEC; ++jj) s_o[j][col0 + jj] = o[jj];
+        for (int jj = 0; jj < G::VEC; ++jj) s_o[j][lcol + jj] = o[jj];
       }
       ss = warp_sum(row0 == 0 ? ss : 0.f);
       if (lane == 0) s_ss[j][warp] = ss;
     }
     __syncthreads();
-
-    // ---- D: gated RMSNorm and the output row, one warp per token
-    if (warp < nt) {
-      const int t = tc0 + warp;
-      float tot = 0.f;
+    if (tid < nt) {
+      float p = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) tot += s_ss[warp][w];
-      const float rinv = rsqrtf(tot * (1.f / kD) + a.norm_eps);
-      const float4 o4 = *reinterpret_cast<const float4*>(&s_o[warp][4 * lane]);
-      const float4 g4 = load4(a.out_gate, (int64_t)t * a.og_rs + (int64_t)h * a.og_hs + 4 * lane, KDA_DT_BF16);
-      float y[4] = {o4.x * rinv * nw.x * sigmoidf_(g4.x), o4.y * rinv * nw.y * sigmoidf_(g4.y),
-                    o4.z * rinv * nw.z * sigmoidf_(g4.z), o4.w * rinv * nw.w * sigmoidf_(g4.w)};
-      store_out<4>(out + (int64_t)t * a.o_rs + 4 * lane, y);
+      for (int w = 0; w < NW; ++w) p += s_ss[tid][w];
+      s_part[tid] = p;
     }
+    if constexpr (CL > 1) {
+      cg::this_cluster().sync();  // every CTA's partial sums are visible cluster-wide
+    } else {
+      __syncthreads();
+    }
+
+    // ---- D: gated RMSNorm of this slab of the outputs
+    for (int i = tid; i < nt * (W / 4); i += NT) {
+      const int j = i / (W / 4), c4 = 4 * (i % (W / 4));
+      float tot = 0.f;
+      if constexpr (CL > 1) {
+        cg::cluster_group cl = cg::this_cluster();
+#pragma unroll
+        for (int r = 0; r < CL; ++r) tot += *cl.map_shared_rank(&s_part[j], r);
+      } else {
+        tot = s_part[j];
+      }
+      const float rinv = rsqrtf(tot * (1.f / kD) + a.norm_eps);
+      const float4 o4 = *reinterpret_cast<const float4*>(&s_o[j][c4]);
+      const uint2 g2 = *reinterpret_cast<const uint2*>(&s_og[j][c4]);
+      const float4 nw = *reinterpret_cast<const float4*>(&s_nw[c4]);
+      float y[4] = {o4.x * rinv * nw.x * sigmoidf_(bf_lo(g2.x)), o4.y * rinv * nw.y * sigmoidf_(bf_hi(g2.x)),
+                    o4.z * rinv * nw.z * sigmoidf_(bf_lo(g2.y)), o4.w * rinv * nw.w * sigmoidf_(bf_hi(g2.y))};
+      store_out<4>(out + (int64_t)(tc0 + j) * a.o_rs + slab0 + c4, y);
+    }
+    if constexpr (CL > 1) cg::this_cluster().sync();  // peers are done reading this CTA's partial sums
   }
 }
 
-cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, cudaStream_t s) {
-  const int64_t blocks = (int64_t)(a.N + 1) * a.H;  // slice N zeroes padding rows
-  if (state_dtype == KDA_DT_F32) {
-    kda_packed_fused_kernel<float><<<dim3((unsigned)blocks), dim3(256), 0, s>>>(a);
-  } else {
-    kda_packed_fused_kernel<__nv_bfloat16><<<dim3((unsigned)blocks), dim3(256), 0, s>>>(a);
+template <typename StateT, int CW, int NW>
+cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, cudaStream_t s) {
+  constexpr int CL = kD / (CW * NW);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((int64_t)(a.N + 1) * a.H * CL));  // slice N zeroes padding rows
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = CL > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kda_packed_fused_kernel<StateT, CW, NW>, a);
+}
+
+template <typename StateT>
+cudaError_t launch_packed_fused_typed(const PackedFusedArgs& a, int cluster, cudaStream_t s) {
+  switch (cluster) {
+    case 1: return launch_packed_fused_variant<StateT, 16, 8>(a, s);
+    case 2: return launch_packed_fused_variant<StateT, 16, 4>(a, s);
+    case 4: return launch_packed_fused_variant<StateT, 16, 2>(a, s);
+    case 8: return launch_packed_fused_variant<StateT, 8, 2>(a, s);
+    default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
+}
+
+cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, int cluster, cudaStream_t s) {
+  if (state_dtype == KDA_DT_F32) return launch_packed_fused_typed<float>(a, cluster, s);
+  return launch_packed_fused_typed<__nv_bfloat16>(a, cluster, s);
 }
 
 }  // namespace kda

@@ -30,6 +30,7 @@ struct PackedFusedArgs {
   float lower_bound, norm_eps, scale;
 };
 
-cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, cudaStream_t s);
+// `cluster` CTAs (1, 2, 4 or 8) share each (sequence, head), one value slab each.
+cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, int cluster, cudaStream_t s);
 
 }  // namespace kda

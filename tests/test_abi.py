@@ -344,6 +344,10 @@ def test_packed_fused_contract(lib):
     assert _call_pf(lib, t) == INVALID
     assert _call_pf(lib, _pf_args(), eps=float("nan")) == INVALID
     t = _pf_args()
+    t["x"] = torch.zeros(5, 3 * 256 + 4, dtype=torch.bfloat16)[:, : 3 * 256]  # rows 8 bytes off 16
+    assert _call_pf(lib, t) == UNSUPPORTED
+    assert "16-byte" in _msg(lib)
+    t = _pf_args()
     t["out"] = t["output_gate"]
     assert _call_pf(lib, t) == ALIAS
     t = _pf_args()
@@ -353,6 +357,19 @@ def test_packed_fused_contract(lib):
     t["raw_beta"] = torch.zeros(0, 2, dtype=torch.bfloat16)
     t["query_start_loc"] = torch.zeros(4, dtype=torch.int32)
     assert _call_pf(lib, t) == OK  # no token rows: nothing to launch
+
+
+def test_packed_fused_cluster_policy(lib):
+    # two CTAs per unit up to a quarter of the SM count in units, one above
+    assert binding.kda_plan_split(4, 12, 0, 1, 152) == 2
+    assert binding.kda_plan_split(4, 38, 0, 1, 152) == 2
+    assert binding.kda_plan_split(4, 96, 0, 1, 152) == 1
+    assert binding.kda_plan_split(4, 1536, 1, 1, 152) == 1
+    assert binding.kda_plan_schedule(4, 12, 0, 1, 152) == 1
+    assert binding.kda_plan_split(5, 12, 0, 1, 152) == 0  # unknown op
+    assert lib.kda_set_split_override(16) == OK
+    assert binding.kda_plan_split(4, 12, 0, 1, 152) == 8  # a forced 16 runs as 8
+    assert lib.kda_set_split_override(0) == OK
 
 
 def test_schedule_override_and_plan(lib):

@@ -40,3 +40,15 @@ def test_recorded_traffic_is_well_formed():
 def test_byte_models():
     # fp32 state, bf16 activations: 2*64 KiB state + 4*256 B vectors + 2 B beta + 256 B out per unit
     assert bench.bytes_t1(1, 0, 1, 4) - bench.bytes_t1(0, 0, 1, 4) == 2 * 128 * 128 * 4 + 4 * 256 + 2 + 256 + 4  # + the slot index
+
+
+def test_packed_fused_byte_model():
+    # one sequence of two tokens, one checkpoint column, H=1, fp32: state and conv
+    # cache read once and written once, two tokens' activations, no padding
+    unit = 128 * 128 * 4 + 3 * 3 * 128 * 2
+    per_tok = 3 * 128 * 2 + 128 * 2 + 2 + 128 * 2 + 128 * 2
+    params = 3 * 4 * 128 * 4 + 4 + 128 * 4 + 128 * 4
+    meta = 2 * 4 + 4 + 4
+    assert bench.bytes_packed_fused([2], 1, 1, 4, 2) == 2 * unit + 2 * per_tok + params + meta
+    # an empty sequence adds only its metadata and padding rows add zero output
+    assert bench.bytes_packed_fused([2, 0], 1, 1, 4, 3) == 2 * unit + 2 * per_tok + 128 * 2 + params + 3 * 4 + 8 + 8

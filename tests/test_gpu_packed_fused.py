@@ -21,6 +21,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 def lib():
     build.build()
     yield binding.library()
+    binding.kda_set_split_override(0)
 
 
 def _run(d, out=None, lower_bound=-5.0):
@@ -72,6 +73,37 @@ def test_packed_fused_config_sweep(N, t_max, state_dtype):
     out = torch.full((case["x"].shape[0], 12, 128), 5.0, dtype=torch.bfloat16, device="cuda")
     _run(d, out=out)
     torch.cuda.synchronize()
+    _check(case, d, st0, cs0, out)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_packed_fused_every_cluster_size(cluster, state_dtype):
+    binding.kda_set_split_override(cluster)
+    try:
+        case = synth.packed_fused_case(7, 5, H=3, seed=60 + cluster, null_count=1, pad_rows=3,
+                                       state_dtype=state_dtype)
+        case["state_indices"][0, 2] = -1  # one skipped checkpoint
+        d, st0, cs0 = _setup(case)
+        out = torch.full((case["x"].shape[0], 3, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+        _run(d, out=out)
+        torch.cuda.synchronize()
+    finally:
+        binding.kda_set_split_override(0)
+    _check(case, d, st0, cs0, out)
+
+
+@pytest.mark.parametrize("cluster", [1, 8])
+def test_packed_fused_long_sequences_every_cluster_extreme(cluster):
+    binding.kda_set_split_override(cluster)
+    try:
+        case = synth.packed_fused_case(3, 17, H=2, seed=70 + cluster, lengths=[17, 9, 12], cols=10,
+                                       accepted=[1, 10, 4])
+        d, st0, cs0 = _setup(case)
+        out = _run(d)
+        torch.cuda.synchronize()
+    finally:
+        binding.kda_set_split_override(0)
     _check(case, d, st0, cs0, out)
 
 
