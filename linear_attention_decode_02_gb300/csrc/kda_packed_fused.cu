@@ -31,8 +31,13 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // =====================================================================================
 // One cluster of CL CTAs per (sequence, head); CTA `rank` owns the value
-// columns [rank*W, rank*W + W), W = CW*NW, warp w a strip of CW of them over
-// all 128 key rows.  The state slab is loaded once from the start slot (the
+// columns [rank*W, rank*W + W).  Column form (ROWSPLIT false): warp w owns a
+// strip of W/NW of them over all 128 key rows, so a token's reductions need
+// no CTA barrier.  Row form (ROWSPLIT true, for the narrow slabs of large
+// clusters): warp w owns key rows [16w, 16w+16) of all W columns and the
+// warps' partial reductions meet in shared memory, one CTA barrier per
+// token; every CTA keeps 8 warps for the conv and coefficient phases while
+// each SM stores only W/128 of the state.  The state slab is loaded once from the start slot (the
 // checkpoint of the last accepted token) and carried in float32 registers
 // across the sequence's tokens; after each token it is stored to that
 // token's checkpoint slot (rounded once if bf16), so a call moves one state
@@ -61,14 +66,17 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 //     outputs.
 // Grid slice n == N zeroes the padding token rows outside [qsl[0], qsl[N]).
 // =====================================================================================
-template <typename StateT, int CW, int NW>
+template <typename StateT, int W, int NW, bool ROWSPLIT>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fused_kernel(const PackedFusedArgs a) {
   constexpr int NT = NW * 32, TC = 8;
-  constexpr int W = CW * NW;       // value columns of this CTA
-  constexpr int CL = kD / W;       // CTAs per (sequence, head)
+  constexpr int CL = kD / W;                 // CTAs per (sequence, head)
+  constexpr int CW = ROWSPLIT ? W : W / NW;  // columns of one warp's strip
   constexpr int NCH = 2 * kD + W;  // conv channels: all of q and k, this slab of v
   constexpr int PT = 48 + W / 4;   // 16-byte staging pieces per token
   using G = Strip<StateT, CW>;
+  // fragments per lane: all 128 rows (column form) or the warp's 16 (row form)
+  constexpr int P = ROWSPLIT ? (kD / NW) / G::RPI : G::PASSES;
+  static_assert(!ROWSPLIT || (kD / NW) % G::RPI == 0, "row form: a warp's rows must tile its passes");
   static_assert(CL * W == kD && (CL == 1 || CL == 2 || CL == 4 || CL == 8), "slabs must tile the 128 columns");
   static_assert(W % 8 == 0, "slabs are staged in 16-byte pieces");
   // The staged conv input (read in phase A) and the raw outputs (written in
@@ -89,6 +97,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   __shared__ float s_ss[TC][NW];                        // per-warp sums of squares
   __shared__ float s_part[TC];                          // this CTA's sum of squares per token
   __shared__ __nv_bfloat16 s_hist[3][NCH];              // raw conv history, oldest first (thread-owned)
+  __shared__ float2 s_red[ROWSPLIT ? 2 : 1][ROWSPLIT ? NW : 1][ROWSPLIT ? W : 1];  // row form: (a, b) partials
 
   const int rank = CL == 1 ? 0 : (int)(blockIdx.x % CL);
   const int unit = blockIdx.x / CL;
@@ -98,16 +107,22 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int lcol = warp * CW + (lane % G::LPR) * G::VEC;  // column within the slab
+  const int lcol = (ROWSPLIT ? 0 : warp * CW) + (lane % G::LPR) * G::VEC;  // column within the slab
   const int col0 = slab0 + lcol;
-  const int row0 = lane / G::LPR;
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD;
+  const int row0 = (ROWSPLIT ? warp * (kD / NW) : 0) + lane / G::LPR;   // rows row0 + i*RPI, i < P
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD + slab0;
+  auto zero_rows = [&](int lo, int hi) {  // this slab of output rows [lo, hi)
+    for (int i = tid; i < (hi - lo) * (W / 4); i += NT) {
+      const float z[4] = {0.f, 0.f, 0.f, 0.f};
+      store_out<4>(out + (int64_t)(lo + i / (W / 4)) * a.o_rs + 4 * (i % (W / 4)), z);
+    }
+  };
 
   if (n == a.N) {  // padding token rows
     const int lo = min(max(__ldg(a.qsl), 0), a.R);
     const int hi = max(min(__ldg(a.qsl + a.N), a.R), lo);
-    for (int t = row0; t < lo; t += G::RPI) store_out_zero<G::VEC>(out + t * a.o_rs + col0);
-    for (int t = hi + row0; t < a.R; t += G::RPI) store_out_zero<G::VEC>(out + t * a.o_rs + col0);
+    zero_rows(0, lo);
+    zero_rows(hi, a.R);
     return;
   }
 
@@ -172,14 +187,22 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   const bool live_acc = acc >= 1 && acc <= a.cols;
   const int s0 = live_acc ? __ldg(row_slots + acc - 1) : 0;
   if (s0 <= 0 || s0 >= a.num_slots) {  // null sequence: zero its rows, touch no cache
-    for (int t = t0 + row0; t < t1; t += G::RPI) store_out_zero<G::VEC>(out + t * a.o_rs + col0);
+    zero_rows(t0, t1);
     cp_async_wait_all();
     return;
   }
 
   const int64_t head_off = (int64_t)h * kD * kD;
-  FltRegs<G> S;
-  strip_load<StateT, G>(static_cast<const StateT*>(a.state) + (int64_t)s0 * a.slot_stride + head_off, row0, col0, S);
+  float2 S[P][G::VEC / 2];  // float32 state fragments: rows row0 + i*RPI, columns col0..col0+VEC
+  {
+    const StateT* sp = static_cast<const StateT*>(a.state) + (int64_t)s0 * a.slot_stride + head_off;
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      const typename Frag<StateT>::Raw r = Frag<StateT>::load(sp + (row0 + i * G::RPI) * kD + col0);
+#pragma unroll
+      for (int q = 0; q < G::VEC / 2; ++q) S[i][q] = Frag<StateT>::get2(r, q);
+    }
+  }
 
   __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
   for (int lc = tid; lc < NCH; lc += NT) {
@@ -253,11 +276,36 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     }
     __syncthreads();
 
-    // ---- C: the chunk's tokens on this warp's strip
+    // ---- C: the chunk's tokens on this warp's fragments
     for (int j = 0; j < nt; ++j) {
       const float2 tk = s_tok[j];
+      const float4* coef = s_coef[j];
+      float2 a2[G::VEC / 2], b2[G::VEC / 2];
+#pragma unroll
+      for (int q = 0; q < G::VEC / 2; ++q) { a2[q] = make_float2(0.f, 0.f); b2[q] = make_float2(0.f, 0.f); }
+#pragma unroll
+      for (int i = 0; i < P; ++i) accumulate_row<G::VEC / 2>(coef[row0 + i * G::RPI], S[i], a2, b2);
       float acc_a[G::VEC], acc_b[G::VEC];
-      strip_reduce<G>(S, s_coef[j], row0, acc_a, acc_b);
+      strip_allreduce<G>(a2, b2, acc_a, acc_b);
+      if constexpr (ROWSPLIT) {  // combine the warps' row partials
+        if (lane < G::LPR) {
+#pragma unroll
+          for (int jj = 0; jj < G::VEC; ++jj) s_red[j & 1][warp][lcol + jj] = make_float2(acc_a[jj], acc_b[jj]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int jj = 0; jj < G::VEC; ++jj) {
+          float ta = 0.f, tb = 0.f;
+#pragma unroll
+          for (int w = 0; w < NW; ++w) {
+            const float2 r = s_red[j & 1][w][lcol + jj];
+            ta += r.x;
+            tb += r.y;
+          }
+          acc_a[jj] = ta;
+          acc_b[jj] = tb;
+        }
+      }
       float u[G::VEC], o[G::VEC];
       float ss = 0.f;
 #pragma unroll
@@ -266,15 +314,26 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
         o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
         ss = fmaf(o[jj], o[jj], ss);
       }
-      strip_update<G>(S, s_coef[j], row0, u);
+      float2 u2[G::VEC / 2];
+      pairs_of<G::VEC>(u, u2);
+#pragma unroll
+      for (int i = 0; i < P; ++i) {
+        const float4 c = coef[row0 + i * G::RPI];
+        update_row<G::VEC / 2>(c.z, c.w, S[i], u2, S[i]);
+      }
       const int sl = s_slot[j];
-      if (sl != 0)
-        strip_store<StateT, G>(static_cast<StateT*>(a.state) + (int64_t)sl * a.slot_stride + head_off, row0, col0, S);
-      if (row0 == 0) {
+      if (sl != 0) {
+        StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sl * a.slot_stride + head_off;
+#pragma unroll
+        for (int i = 0; i < P; ++i) Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(S[i]));
+      }
+      // lanes of the first row of each strip hold distinct columns (row form: warp 0 only)
+      const bool writer = (lane < G::LPR) && (!ROWSPLIT || warp == 0);
+      if (writer) {
 #pragma unroll
         for (int jj = 0; jj < G::VEC; ++jj) s_o[j][lcol + jj] = o[jj];
       }
-      ss = warp_sum(row0 == 0 ? ss : 0.f);
+      ss = warp_sum(writer ? ss : 0.f);
       if (lane == 0) s_ss[j][warp] = ss;
     }
     __syncthreads();
@@ -307,15 +366,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
       const float4 nw = *reinterpret_cast<const float4*>(&s_nw[c4]);
       float y[4] = {o4.x * rinv * nw.x * sigmoidf_(bf_lo(g2.x)), o4.y * rinv * nw.y * sigmoidf_(bf_hi(g2.x)),
                     o4.z * rinv * nw.z * sigmoidf_(bf_lo(g2.y)), o4.w * rinv * nw.w * sigmoidf_(bf_hi(g2.y))};
-      store_out<4>(out + (int64_t)(tc0 + j) * a.o_rs + slab0 + c4, y);
+      store_out<4>(out + (int64_t)(tc0 + j) * a.o_rs + c4, y);
     }
     if constexpr (CL > 1) cg::this_cluster().sync();  // peers are done reading this CTA's partial sums
   }
 }
 
-template <typename StateT, int CW, int NW>
+template <typename StateT, int W, int NW, bool ROWSPLIT>
 cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, cudaStream_t s) {
-  constexpr int CL = kD / (CW * NW);
+  constexpr int CL = kD / W;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((int64_t)(a.N + 1) * a.H * CL));  // slice N zeroes padding rows
   cfg.blockDim = dim3(NW * 32);
@@ -328,16 +387,16 @@ cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, cudaStream_t s
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CL > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kda_packed_fused_kernel<StateT, CW, NW>, a);
+  return cudaLaunchKernelEx(&cfg, kda_packed_fused_kernel<StateT, W, NW, ROWSPLIT>, a);
 }
 
 template <typename StateT>
 cudaError_t launch_packed_fused_typed(const PackedFusedArgs& a, int cluster, cudaStream_t s) {
   switch (cluster) {
-    case 1: return launch_packed_fused_variant<StateT, 16, 8>(a, s);
-    case 2: return launch_packed_fused_variant<StateT, 16, 4>(a, s);
-    case 4: return launch_packed_fused_variant<StateT, 16, 2>(a, s);
-    case 8: return launch_packed_fused_variant<StateT, 8, 2>(a, s);
+    case 1: return launch_packed_fused_variant<StateT, 128, 8, false>(a, s);
+    case 2: return launch_packed_fused_variant<StateT, 64, 4, false>(a, s);
+    case 4: return launch_packed_fused_variant<StateT, 32, 8, true>(a, s);
+    case 8: return launch_packed_fused_variant<StateT, 16, 8, true>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -360,9 +360,10 @@ def test_packed_fused_contract(lib):
 
 
 def test_packed_fused_cluster_policy(lib):
-    # two CTAs per unit up to a quarter of the SM count in units, one above
-    assert binding.kda_plan_split(4, 12, 0, 1, 152) == 2
-    assert binding.kda_plan_split(4, 38, 0, 1, 152) == 2
+    # eight CTAs per unit up to an eighth of the SM count in units, one above
+    assert binding.kda_plan_split(4, 12, 0, 1, 152) == 8
+    assert binding.kda_plan_split(4, 19, 0, 1, 152) == 8
+    assert binding.kda_plan_split(4, 20, 0, 1, 152) == 1
     assert binding.kda_plan_split(4, 96, 0, 1, 152) == 1
     assert binding.kda_plan_split(4, 1536, 1, 1, 152) == 1
     assert binding.kda_plan_schedule(4, 12, 0, 1, 152) == 1
