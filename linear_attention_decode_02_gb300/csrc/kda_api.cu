@@ -689,7 +689,7 @@ kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_w
   a.gate_mode = has_lower_bound ? kda::KDA_GATE_LOWER_BOUND : kda::KDA_GATE_SOFTPLUS;
   a.lower_bound = lower_bound; a.norm_eps = norm_eps;
   a.scale = 0.08838834764831845f;  // 1/sqrt(128)
-  return check_launch(kda::launch_packed_fused(a, S.dtype, cluster, st));
+  return check_launch(kda::launch_packed_fused(a, S.dtype, cluster, dev.sms, st));
 }
 
 }  // extern "C"

@@ -2,6 +2,8 @@
 // T >= 1 token rows per sequence) with per-token checkpoints of both caches.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "kda_kernels.cuh"
 #include "kda_packed_fused.h"
 
@@ -23,6 +25,10 @@ __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
                "l"(src)
                : "memory");
+}
+// Hint: bring the 128-byte line holding `p` (a global address) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -100,9 +106,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   __shared__ float2 s_red[ROWSPLIT ? 2 : 1][ROWSPLIT ? NW : 1][ROWSPLIT ? W : 1];  // row form: (a, b) partials
 
   const int rank = CL == 1 ? 0 : (int)(blockIdx.x % CL);
-  const int unit = blockIdx.x / CL;
-  const int h = unit % a.H;
-  const int n = unit / a.H;
   const int slab0 = rank * W;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -110,6 +113,20 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   const int lcol = (ROWSPLIT ? 0 : warp * CW) + (lane % G::LPR) * G::VEC;  // column within the slab
   const int col0 = slab0 + lcol;
   const int row0 = (ROWSPLIT ? warp * (kD / NW) : 0) + lane / G::LPR;   // rows row0 + i*RPI, i < P
+  const int HD = a.H * kD;
+  // Section and channel-within-section of local conv channel lc.
+  auto sec_of = [](int lc) { return lc < kD ? 0 : (lc < 2 * kD ? 1 : 2); };
+  auto cis_of = [slab0](int lc) { return lc < 2 * kD ? (lc & (kD - 1)) : slab0 + lc - 2 * kD; };
+  __shared__ int4 s_pf;  // next unit: (start slot or 0, first token, end token, head)
+
+  // Persistent: each cluster walks the units (sequence, head) with a stride
+  // of the grid's cluster count; the padding slice is unit N*H .. (N+1)*H-1.
+  const int num_units = (a.N + 1) * a.H;
+  const int unit_stride = gridDim.x / CL;
+  for (int unit = blockIdx.x / CL; unit < num_units; unit += unit_stride) {
+  const int h = unit % a.H;
+  const int n = unit / a.H;
+  __syncthreads();  // the previous unit is done with the shared arrays
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD + slab0;
   auto zero_rows = [&](int lo, int hi) {  // this slab of output rows [lo, hi)
     for (int i = tid; i < (hi - lo) * (W / 4); i += NT) {
@@ -123,13 +140,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     const int hi = max(min(__ldg(a.qsl + a.N), a.R), lo);
     zero_rows(0, lo);
     zero_rows(hi, a.R);
-    return;
+    continue;
   }
-
-  const int HD = a.H * kD;
-  // Section and channel-within-section of local conv channel lc.
-  auto sec_of = [](int lc) { return lc < kD ? 0 : (lc < 2 * kD ? 1 : 2); };
-  auto cis_of = [slab0](int lc) { return lc < 2 * kD ? (lc & (kD - 1)) : slab0 + lc - 2 * kD; };
 
   // Parameters first: they depend on nothing, so their copies overlap the
   // metadata loads below.
@@ -150,9 +162,18 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   const int t1 = min(__ldg(a.qsl + n + 1), a.R);
   const int acc = __ldg(a.accepted + n);
   int slot = (tid < TC && tid < a.cols) ? __ldg(row_slots + tid) : 0;  // first chunk's checkpoints
+  // The next unit this CTA runs: its metadata now, its slot during phase A.
+  const int next = unit + unit_stride;
+  const int next_n = next / a.H;
+  int pf_t0 = 0, pf_t1 = 0, pf_acc = 0, pf_slot = 0;
+  if (tid == 0 && next_n < a.N) {
+    pf_t0 = max(__ldg(a.qsl + next_n), 0);
+    pf_t1 = min(__ldg(a.qsl + next_n + 1), a.R);
+    pf_acc = __ldg(a.accepted + next_n);
+  }
   if (t1 <= t0) {  // empty sequence: nothing written
     cp_async_wait_all();
-    return;
+    continue;
   }
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(a.x);
   const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(a.gate);
@@ -189,7 +210,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   if (s0 <= 0 || s0 >= a.num_slots) {  // null sequence: zero its rows, touch no cache
     zero_rows(t0, t1);
     cp_async_wait_all();
-    return;
+    continue;
   }
 
   const int64_t head_off = (int64_t)h * kD * kD;
@@ -230,6 +251,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     }
     __syncthreads();
 
+    if (tid == 0 && tc0 == t0 && next_n < a.N && pf_t1 > pf_t0 && pf_acc >= 1 && pf_acc <= a.cols)
+      pf_slot = __ldg(a.idx + (int64_t)next_n * a.idx_rs + pf_acc - 1);
     // ---- A: conv + SiLU and this CTA's share of the conv checkpoints
     for (int lc = tid; lc < NCH; lc += NT) {
       const int sec = sec_of(lc), cis = cis_of(lc);
@@ -259,7 +282,38 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
       s_hist[1][lc] = h1;
       s_hist[2][lc] = h2;
     }
+    if (tid == 0 && tc0 == t0)
+      s_pf = make_int4(pf_slot > 0 && pf_slot < a.num_slots ? pf_slot : 0, pf_t0, min(pf_t1, pf_t0 + TC),
+                       next % a.H);
     __syncthreads();
+
+    // Prefetch the next unit's state block, conv history and first token rows
+    // into L2, overlapping this unit's checkpoint stores.
+    if (tc0 == t0 && s_pf.x != 0) {
+      const int4 pf = s_pf;
+      const char* sb = reinterpret_cast<const char*>(static_cast<const StateT*>(a.state) +
+                                                     (int64_t)pf.x * a.slot_stride + (int64_t)pf.w * kD * kD);
+      constexpr int NL = kD * kD * (int)sizeof(StateT) / 128;  // 128-byte lines of a state block
+      for (int i = rank * (NL / CL) + tid; i < (rank + 1) * (NL / CL); i += NT) prefetch_l2(sb + (int64_t)i * 128);
+      if (rank == 0) {
+        const int ntok = pf.z - pf.y;
+        for (int i = tid; i < ntok * 10 + 18; i += NT) {
+          const __nv_bfloat16* line;
+          if (i < ntok * 10) {
+            const int64_t t = pf.y + i / 10;
+            const int c = i % 10;
+            if (c < 6) line = xb + t * a.x_rs + (int64_t)(c >> 1) * HD + pf.w * kD + (c & 1) * 64;
+            else if (c < 8) line = gb + t * a.g_rs + (int64_t)pf.w * a.g_hs + (c - 6) * 64;
+            else line = ogb + t * a.og_rs + (int64_t)pf.w * a.og_hs + (c - 8) * 64;
+          } else {
+            const int c = i - ntok * 10;  // tap c / 6, section (c % 6) / 2, half c % 2
+            line = cs + (int64_t)pf.x * a.cs_slot_stride + (int64_t)(c / 6) * a.cs_tap_stride +
+                   (int64_t)((c % 6) >> 1) * HD + pf.w * kD + (c & 1) * 64;
+          }
+          prefetch_l2(line);
+        }
+      }
+    }
 
     // ---- B: per-token decays and coefficients
     for (int j = warp; j < nt; j += NW) {
@@ -370,13 +424,24 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     }
     if constexpr (CL > 1) cg::this_cluster().sync();  // peers are done reading this CTA's partial sums
   }
+  }  // units
 }
 
 template <typename StateT, int W, int NW, bool ROWSPLIT>
-cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, cudaStream_t s) {
+cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, int sms, cudaStream_t s) {
   constexpr int CL = kD / W;
+  auto kernel = kda_packed_fused_kernel<StateT, W, NW, ROWSPLIT>;
+  const int64_t units = (int64_t)(a.N + 1) * a.H;  // unit N*H.. is the padding slice
+  int64_t clusters = units;
+  if (CL == 1) {  // persistent: as many CTAs as fit on the device at once
+    static const int per_sm = [&] {
+      int b = 0;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, NW * 32, 0) == cudaSuccess && b > 0 ? b : 1;
+    }();
+    clusters = std::min<int64_t>(units, (int64_t)per_sm * sms);
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((int64_t)(a.N + 1) * a.H * CL));  // slice N zeroes padding rows
+  cfg.gridDim = dim3((unsigned)(clusters * CL));
   cfg.blockDim = dim3(NW * 32);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
@@ -387,23 +452,23 @@ cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, cudaStream_t s
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = CL > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kda_packed_fused_kernel<StateT, W, NW, ROWSPLIT>, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
 template <typename StateT>
-cudaError_t launch_packed_fused_typed(const PackedFusedArgs& a, int cluster, cudaStream_t s) {
+cudaError_t launch_packed_fused_typed(const PackedFusedArgs& a, int cluster, int sms, cudaStream_t s) {
   switch (cluster) {
-    case 1: return launch_packed_fused_variant<StateT, 128, 8, false>(a, s);
-    case 2: return launch_packed_fused_variant<StateT, 64, 4, false>(a, s);
-    case 4: return launch_packed_fused_variant<StateT, 32, 8, true>(a, s);
-    case 8: return launch_packed_fused_variant<StateT, 16, 8, true>(a, s);
+    case 1: return launch_packed_fused_variant<StateT, 128, 8, false>(a, sms, s);
+    case 2: return launch_packed_fused_variant<StateT, 64, 4, false>(a, sms, s);
+    case 4: return launch_packed_fused_variant<StateT, 32, 8, true>(a, sms, s);
+    case 8: return launch_packed_fused_variant<StateT, 16, 8, true>(a, sms, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, int cluster, cudaStream_t s) {
-  if (state_dtype == KDA_DT_F32) return launch_packed_fused_typed<float>(a, cluster, s);
-  return launch_packed_fused_typed<__nv_bfloat16>(a, cluster, s);
+cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, int cluster, int sms, cudaStream_t s) {
+  if (state_dtype == KDA_DT_F32) return launch_packed_fused_typed<float>(a, cluster, sms, s);
+  return launch_packed_fused_typed<__nv_bfloat16>(a, cluster, sms, s);
 }
 
 }  // namespace kda

@@ -30,7 +30,8 @@ struct PackedFusedArgs {
   float lower_bound, norm_eps, scale;
 };
 
-// `cluster` CTAs (1, 2, 4 or 8) share each (sequence, head), one value slab each.
-cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, int cluster, cudaStream_t s);
+// `cluster` CTAs (1, 2, 4 or 8) share each (sequence, head), one value slab
+// each; with one, the grid is persistent (sized from `sms`).
+cudaError_t launch_packed_fused(const PackedFusedArgs& a, int state_dtype, int cluster, int sms, cudaStream_t s);
 
 }  // namespace kda
