@@ -29,7 +29,7 @@ def test_recorded_traffic_is_well_formed():
     with open(path) as f:
         rec = json.load(f)
     for kind, e in rec["kernels"].items():
-        assert e["source"] in bench.SPLIT_SOURCE.values() or e["source"] == "kda_stream.cu", kind
+        assert e["source"].endswith(".cu") and os.path.isfile(os.path.join(bench.CSRC, e["source"])), kind
         assert e["dram_bytes_per_launch"] == e["dram_read_per_launch"] + e["dram_write_per_launch"]
         assert "--clock-control none" in e["command"]
         got = bench.ncu_traffic(kind)
