@@ -223,3 +223,19 @@ def test_packed_fused_equals_token_by_token_fused_calls():
         L = int(qsl[n + 1]) - int(qsl[n])
         last = int(idx[n, L - 1])
         assert (d["state"][last] - d2["state"][int(idx[n, 0])]).abs().max().item() <= P.F32_STATE_ATOL
+
+
+@pytest.mark.parametrize("H,state_dtype", [(12, torch.float32), (12, torch.bfloat16), (24, torch.float32)])
+def test_packed_fused_full_size_sampled(H, state_dtype):
+    """The timed configuration: 128 sequences of 5 tokens, one accepted token,
+    a checkpoint per token; the oracle checks 12 sampled sequences, the rest
+    through the untouched-slot and padding checks."""
+    N, T = 128, 5
+    case = synth.packed_fused_case(N, T, H=H, seed=80 + H, lengths=[T] * N, accepted=1, state_dtype=state_dtype)
+    d, st0, cs0 = _setup(case)
+    out = torch.full((N * T, H, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    _run(d, out=out)
+    torch.cuda.synchronize()
+    assert not torch.isnan(out).any()  # every token row written
+    seqs = sorted(np.random.default_rng(H).choice(N, 12, replace=False).tolist())
+    _check(case, d, st0, cs0, out, seqs=seqs)
