@@ -52,3 +52,11 @@ def test_packed_fused_byte_model():
     assert bench.bytes_packed_fused([2], 1, 1, 4, 2) == 2 * unit + 2 * per_tok + params + meta
     # an empty sequence adds only its metadata and padding rows add zero output
     assert bench.bytes_packed_fused([2, 0], 1, 1, 4, 3) == 2 * unit + 2 * per_tok + 128 * 2 + params + 3 * 4 + 8 + 8
+
+
+def test_oracle_baseline_runs_on_several_single_threaded_processes():
+    (g1, r1, e1), per_step, procs = bench.oracle_rates(0.4, H=2, workers=2, steps=2)
+    assert procs == 2 and len(per_step) == 2
+    assert g1 > 0 and r1 >= 8 and e1 >= 0.2
+    for g, r, e in per_step:
+        assert g > 0 and r >= 16 and e >= 0.2
