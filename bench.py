@@ -16,7 +16,7 @@ ms_per_step is the time per call.  The line also carries the same metric end
 to end (pinned host inputs copied in and the output copied out each step),
 the roofline of the kernel against the measured copy bandwidth, the SM clocks
 seen during the timed region, per-path / per-batch CUDA-graph measurements of
-the four entry points (L2 flushed between replays), and the float64 oracle
+the decode entry points (L2 flushed between replays), and the float64 oracle
 timed on the host cores.
 
 Multi-GPU: every rank runs its own replica (the decode units are independent
@@ -437,6 +437,21 @@ def time_direct(fn, steps, warmup, barrier):
     return e0.elapsed_time(e1) / steps, (wall0, wall1)
 
 
+class L2Flush:
+    """Cold-L2 preparation before a timed replay: write a buffer larger than
+    L2, then read a second one, so the written lines are back in DRAM before
+    the timed region starts (otherwise the kernel pays the flush's own
+    write-backs) and L2 holds none of the kernel's data."""
+
+    def __init__(self):
+        self.w = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        self.r = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    def __call__(self, value):
+        self.w.fill_(value)
+        return self.r.sum()
+
+
 def time_graph(wl, n_calls, reps, flush):
     """Per-call ms of a CUDA graph of `n_calls` launches on rotating slot sets, L2 flushed before each replay."""
     g = torch.cuda.CUDAGraph()
@@ -451,7 +466,7 @@ def time_graph(wl, n_calls, reps, flush):
             wl.step(i)
     times = []
     for r in range(reps + 2):
-        flush.fill_(float(r))
+        flush(float(r))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         g.replay()
@@ -708,7 +723,7 @@ def main():
 
     paths = None
     if not args.no_paths and rank == 0:
-        flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+        flush = L2Flush()
         paths = path_measurements(flush, peak)
         del flush
 
