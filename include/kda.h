@@ -22,9 +22,12 @@
  *        conv + KDA + gated RMSNorm contract.
  *   [P3] "feat(cake_kda): add serving-native packed decode backend" ("Exact
  *        contract"): the packed Kimi K3 T=1 contract.
- *   [P4] "feat(kda): add fused speculative decode kernel - #4809" (review
- *        of the T=1 row mapping): token rows past the last sequence are
- *        padding that write zero and touch no slot.
+ *   [P4] "feat(kda): add fused speculative decode kernel - #4809": the
+ *        packed fused operation (description) that updates conv and
+ *        recurrent caches from accepted-token metadata; the review of the
+ *        T=1 row mapping (token rows past the last sequence are padding
+ *        that write zero and touch no slot); the bf16-state follow-up
+ *        (float32 recurrence across tokens, one rounding per checkpoint).
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -39,7 +42,8 @@
  *   rank, shape, stride, alignment, aliasing) is detected on the host and
  *   returned as a status WITHOUT launching anything; kda_last_error_message()
  *   then describes it.  A launch failure returns KDA_ERR_CUDA.
- * - state_indices: contiguous int32, one entry per decode row.  A row whose
+ * - state_indices: contiguous int32, one entry per decode row (per sequence
+ *   and checkpoint column for kda_packed_fused_decode).  A row whose
  *   index is <= 0 or >= num_slots is a null row: its output is zero and no
  *   cache slot is read or written (slot 0 is the reserved null slot).  Live
  *   indices must be unique; that is a caller contract the library does not
