@@ -239,3 +239,28 @@ def test_packed_fused_full_size_sampled(H, state_dtype):
     assert not torch.isnan(out).any()  # every token row written
     seqs = sorted(np.random.default_rng(H).choice(N, 12, replace=False).tolist())
     _check(case, d, st0, cs0, out, seqs=seqs)
+
+
+def test_packed_fused_no_sequences_all_rows_padding():
+    """N = 0 with token rows present: every row is padding, no cache touched."""
+    case = synth.packed_fused_case(1, 1, H=2, seed=97, lengths=[0], pad_rows=3)
+    case["state_indices"] = case["state_indices"][:0]
+    case["num_accepted_tokens"] = case["num_accepted_tokens"][:0]
+    case["query_start_loc"] = torch.zeros(1, dtype=torch.int32)
+    d, st0, cs0 = _setup(case)
+    out = torch.full((3, 2, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    _run(d, out=out)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+    assert torch.equal(st0, d["state"]) and torch.equal(cs0, d["conv_state"])
+
+
+def test_packed_fused_every_start_slot_null():
+    case = synth.packed_fused_case(6, 3, H=4, seed=98)
+    case["state_indices"][:] = -1
+    d, st0, cs0 = _setup(case)
+    out = torch.full((case["x"].shape[0], 4, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    _run(d, out=out)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+    assert torch.equal(st0, d["state"]) and torch.equal(cs0, d["conv_state"])

@@ -179,3 +179,16 @@ def test_spec_graph_replay_with_dynamic_cu_seqlens():
     # token row 1 belongs to sequence 2 (slot 3); row 2 is padding
     assert not torch.equal(fresh[3], d["state"][3]) and torch.equal(fresh[2], d["state"][2])
     assert torch.count_nonzero(out[2]) == 0
+
+
+def test_spec_no_rows_all_token_rows_padding():
+    case = synth.spec_case(1, 1, seed=12, H=2, lengths=[0], pad_rows=4, num_slots=4)
+    case["state_indices"] = case["state_indices"][:0]
+    case["cu_seqlens"] = torch.zeros(1, dtype=torch.int32)
+    d = P.to_device(case)
+    before = d["state"].clone()
+    out = torch.full((4, 2, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    _run(d, 1, out=out)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+    assert torch.equal(before, d["state"])

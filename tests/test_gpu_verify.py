@@ -193,3 +193,18 @@ def test_verify_argument_errors():
         _run(d, 3, bad, None)
     with pytest.raises(binding.KdaError):
         _run(d, 3, d["state"].view(M, 2, 128, 128)[:, :, :3, :], None)
+
+
+def test_verify_no_rows_all_token_rows_padding():
+    case = synth.spec_case(1, 1, seed=18, H=2, lengths=[0], pad_rows=3, num_slots=4)
+    case["state_indices"] = case["state_indices"][:0]
+    case["cu_seqlens"] = torch.zeros(1, dtype=torch.int32)
+    d = P.to_device(case)
+    before = d["state"].clone()
+    corr, kg = _caches(4, 2, 2)
+    out = torch.full((3, 2, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    _run(d, 1, corr, kg, out=out)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out) == 0
+    assert torch.equal(before, d["state"])
+    assert torch.isnan(corr).all() and torch.isnan(kg).all()
