@@ -208,3 +208,15 @@ def test_verify_no_rows_all_token_rows_padding():
     assert torch.count_nonzero(out) == 0
     assert torch.equal(before, d["state"])
     assert torch.isnan(corr).all() and torch.isnan(kg).all()
+
+
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_verify_full_size(state_dtype):
+    """N=128 rows of up to 16 tokens (H=16) from a read-only pool of either dtype."""
+    case = synth.spec_case(128, 16, seed=22, null_count=8, state_dtype=state_dtype)
+    d = P.to_device(case)
+    before = d["state"].clone()
+    corr, kg = _caches(case["state"].shape[0], 16, 16)
+    out = _run(d, 16, corr, kg)
+    torch.cuda.synchronize()
+    _check(case, d, before, out, corr, kg, 16)
