@@ -5,6 +5,7 @@ Shapes: the tiny 4-row case, Kimi-Linear H=32 fp32 state (B up to 512 over a
 contract (H=12, bf16 state, 10% padding rows, B from 1 to 512).
 """
 
+import os
 import numpy as np
 import pytest
 import torch
@@ -359,3 +360,18 @@ def test_stream_guard_bands_between_slots(stream_schedule, state_dtype):
     assert torch.equal(buf.view(N, stride)[:, block:], gaps)
     _check_recurrent(case, d, before, out)
     assert binding.kda_device_error() == 0
+
+
+def test_readme_example_runs():
+    """The usage example in the README executes and updates the state in place."""
+    import re as _re
+    with open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "README.md")) as f:
+        blocks = _re.findall(r"```python\n(.*?)```", f.read(), _re.S)
+    assert len(blocks) == 1
+    scope = {}
+    exec(compile(blocks[0], "README.md", "exec"), scope)
+    torch.cuda.synchronize()
+    out, state = scope["out"], scope["state"]
+    assert out.shape == (8, 32, 128) and out.dtype == torch.bfloat16
+    assert torch.isfinite(out.float()).all()
+    assert torch.count_nonzero(state[1:9]) > 0 and torch.count_nonzero(state[0]) == 0
