@@ -481,18 +481,38 @@ def e2e(wl, steps, warmup, barrier):
     """The same call end to end: every step copies its activations and slot
     indices from pinned host memory to the device and its output back.
 
-    The steps are pipelined the way a serving loop would run them: inputs
-    and outputs are double-buffered on the device, host-to-device copies run
-    on one side stream and device-to-host copies on another, and events keep
+    The steps are pipelined the way a serving loop would run them: a step's
+    inputs sit in one pinned staging buffer and cross in one host-to-device
+    copy (the entry point then takes views into the device copy); inputs and
+    outputs are double-buffered on the device, host-to-device copies run on
+    one side stream and device-to-host copies on another, and events keep
     step i's copies ordered with its kernel; the state pool is updated in
     place on the compute stream, so kernels stay in order.
     """
-    keys = wl.e2e_keys
+    keys = list(wl.e2e_keys)
     nb = 2
-    host = [{k: wl.d[k].cpu().pin_memory() for k in keys} for _ in range(nb)]
-    host_idx = [s.cpu().pin_memory() for s in wl.sets]
-    dev = [{k: wl.d[k].clone() for k in keys} for _ in range(nb)]
-    dev_idx = [torch.empty_like(wl.sets[0]) for _ in range(nb)]
+    # staging layout: each input and the slot indices at 256-byte aligned offsets
+    fields, off = [], 0
+    for k in keys + ["__idx__"]:
+        t = wl.sets[0] if k == "__idx__" else wl.d[k]
+        nbytes = t.numel() * t.element_size()
+        fields.append((k, off, nbytes, t.dtype, tuple(t.shape)))
+        off += (nbytes + 255) // 256 * 256
+    total = off
+
+    def views(buf):
+        return {k: buf[o:o + n].view(dt).view(shape) for k, o, n, dt, shape in fields}
+
+    host = []
+    for idx in wl.sets:  # one staging buffer per slot set: the step's inputs as they arrive
+        hb = torch.empty(total, dtype=torch.uint8).pin_memory()
+        hv = views(hb)
+        for k in keys:
+            hv[k].copy_(wl.d[k].cpu())
+        hv["__idx__"].copy_(idx.cpu())
+        host.append(hb)
+    dev = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(nb)]
+    dv = [views(d) for d in dev]
     outs = [torch.empty_like(wl.out) for _ in range(nb)]
     out_h = [torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory() for _ in range(nb)]
     comp = torch.cuda.current_stream()
@@ -506,15 +526,13 @@ def e2e(wl, steps, warmup, barrier):
         b = i % nb
         s_in.wait_event(ev_k[b])  # the kernel two steps back has read this input buffer
         with torch.cuda.stream(s_in):
-            for k in keys:
-                dev[b][k].copy_(host[b][k], non_blocking=True)
-            dev_idx[b].copy_(host_idx[i % len(host_idx)], non_blocking=True)
+            dev[b].copy_(host[i % len(host)], non_blocking=True)
         ev_in[b].record(s_in)
         comp.wait_event(ev_in[b])
         comp.wait_event(ev_out[b])  # the output buffer has been copied out
-        wl.d = {**base, **dev[b]}
+        wl.d = {**base, **{k: dv[b][k] for k in keys}}
         wl.out = outs[b]
-        wl.call(dev_idx[b])
+        wl.call(dv[b]["__idx__"])
         ev_k[b].record(comp)
         s_out.wait_event(ev_k[b])
         with torch.cuda.stream(s_out):
@@ -535,11 +553,9 @@ def e2e(wl, steps, warmup, barrier):
     torch.cuda.synchronize()
     barrier()
     wl.d = base
-    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in keys) + host_idx[0].numel() * 4
+    h2d = sum(n for _, _, n, _, _ in fields)
     d2h = out_h[0].numel() * out_h[0].element_size()
     return e0.elapsed_time(e1) / steps, h2d, d2h
-
-
 def path_measurements(flush, peak):
     """CUDA-graph timings of the decode entry points over their configured sizes."""
     res = {}
