@@ -27,6 +27,42 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
 
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)r * a.H + h) * kD;
   const int slot = __ldg(a.idx + r);
+
+  // Operands that do not depend on the slot are requested before the slot
+  // index resolves, so their round trips overlap it: the conv input x and
+  // taps of this thread's (at most two) channels, the gate, beta, and the
+  // epilogue's norm weight and output gate.
+  const int HD = a.H * kD;
+  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(a.x) + (int64_t)r * a.x_rs;
+  constexpr int CPT = (3 * kD + NT - 1) / NT;  // channels per thread
+  __nv_bfloat16 xb[CPT];
+  float cw[CPT][4];
+#pragma unroll
+  for (int i = 0; i < CPT; ++i) {
+    const int lc = tid + i * NT;
+    if (lc < 3 * kD) {
+      const int sec = lc >> 7;
+      const int ch = sec * HD + h * kD + (lc & (kD - 1));
+      xb[i] = xr[ch];
+      const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + (lc & (kD - 1));
+#pragma unroll
+      for (int t = 0; t < 4; ++t) cw[i][t] = __ldg(w + t * HD);
+    }
+  }
+  float graw = 0.f, gA = 0.f;
+  if (tid < kD) {
+    gA = __ldg(a.A_log + h);
+    graw = __bfloat162float(static_cast<const __nv_bfloat16*>(a.gate)[(int64_t)r * a.g_rs +
+                                                                     (int64_t)h * a.g_hs + tid]) +
+           __ldg(a.dt_bias + h * kD + tid);
+  }
+  const float braw =
+      __bfloat162float(static_cast<const __nv_bfloat16*>(a.beta)[(int64_t)r * a.b_rs + (int64_t)h * a.b_hs]);
+  float nw[G::VEC], og[G::VEC];
+#pragma unroll
+  for (int j = 0; j < G::VEC; ++j) nw[j] = __ldg(a.norm_w + col0 + j);
+  load_cols<G::VEC>(a.out_gate, (int64_t)r * a.og_rs + (int64_t)h * a.og_hs + col0, KDA_DT_BF16, og);
+
   if (slot <= 0 || slot >= a.num_slots) {  // null row: zero output, neither cache touched
     if (row0 == 0) store_out_zero<G::VEC>(out + col0);
     return;
@@ -39,41 +75,28 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
   // Short conv over [cache0, cache1, cache2, x] (oldest first) for the 384
   // channels of this head, then the cache shift.  Each channel is read and
   // written by the same thread; heads own disjoint channels.
-  const int HD = a.H * kD;
-  const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(a.x) + (int64_t)r * a.x_rs;
   __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state) + (int64_t)slot * a.cs_slot_stride;
-  for (int lc = tid; lc < 3 * kD; lc += NT) {
-    const int sec = lc >> 7;
-    const int ch = sec * HD + h * kD + (lc & (kD - 1));
-    const __nv_bfloat16 xb = xr[ch];
-    __nv_bfloat16* cp = cs + ch;
-    const __nv_bfloat16 c0 = cp[0];
-    const __nv_bfloat16 c1 = cp[a.cs_tap_stride];
-    const __nv_bfloat16 c2 = cp[2 * a.cs_tap_stride];
-    const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + (lc & (kD - 1));
-    float y = __ldg(w) * __bfloat162float(c0);
-    y = fmaf(__ldg(w + HD), __bfloat162float(c1), y);
-    y = fmaf(__ldg(w + 2 * HD), __bfloat162float(c2), y);
-    y = fmaf(__ldg(w + 3 * HD), __bfloat162float(xb), y);
-    s_a[lc] = y * sigmoidf_(y);
-    cp[0] = c1;
-    cp[a.cs_tap_stride] = c2;
-    cp[2 * a.cs_tap_stride] = xb;
-  }
-  if (tid < kD) {
-    const float A = expf(__ldg(a.A_log + h));
-    const float x = __bfloat162float(static_cast<const __nv_bfloat16*>(a.gate)[(int64_t)r * a.g_rs +
-                                                                                (int64_t)h * a.g_hs + tid]) +
-                    __ldg(a.dt_bias + h * kD + tid);
-    s_d[tid] = expf(log_decay(x, A, a.gate_mode, a.lower_bound));
-  }
-  const float beta = sigmoidf_(
-      __bfloat162float(static_cast<const __nv_bfloat16*>(a.beta)[(int64_t)r * a.b_rs + (int64_t)h * a.b_hs]));
-  // Epilogue operands, loaded early.
-  float nw[G::VEC], og[G::VEC];
 #pragma unroll
-  for (int j = 0; j < G::VEC; ++j) nw[j] = __ldg(a.norm_w + col0 + j);
-  load_cols<G::VEC>(a.out_gate, (int64_t)r * a.og_rs + (int64_t)h * a.og_hs + col0, KDA_DT_BF16, og);
+  for (int i = 0; i < CPT; ++i) {
+    const int lc = tid + i * NT;
+    if (lc < 3 * kD) {
+      const int ch = (lc >> 7) * HD + h * kD + (lc & (kD - 1));
+      __nv_bfloat16* cp = cs + ch;
+      const __nv_bfloat16 c0 = cp[0];
+      const __nv_bfloat16 c1 = cp[a.cs_tap_stride];
+      const __nv_bfloat16 c2 = cp[2 * a.cs_tap_stride];
+      float y = cw[i][0] * __bfloat162float(c0);
+      y = fmaf(cw[i][1], __bfloat162float(c1), y);
+      y = fmaf(cw[i][2], __bfloat162float(c2), y);
+      y = fmaf(cw[i][3], __bfloat162float(xb[i]), y);
+      s_a[lc] = y * sigmoidf_(y);
+      cp[0] = c1;
+      cp[a.cs_tap_stride] = c2;
+      cp[2 * a.cs_tap_stride] = xb[i];
+    }
+  }
+  if (tid < kD) s_d[tid] = expf(log_decay(graw, expf(gA), a.gate_mode, a.lower_bound));
+  const float beta = sigmoidf_(braw);
   __syncthreads();
 
   const float4 q = *reinterpret_cast<const float4*>(s_a + 4 * lane);
