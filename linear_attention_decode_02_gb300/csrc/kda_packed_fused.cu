@@ -33,6 +33,35 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// Normalises one token's q and k (lane holds key rows 4*lane .. 4*lane+3),
+// writes the per-row coefficient pairs (d k_hat, d q_hat) to cab and
+// (d, k_hat) to cdk, and returns q_hat . k_hat.
+__device__ __forceinline__ float token_coefficient_pairs(float4 q, float4 k, float4 d, int lane, float2* cab,
+                                                         float2* cdk) {
+  float qq = q.x * q.x + q.y * q.y + q.z * q.z + q.w * q.w;
+  float kk = k.x * k.x + k.y * k.y + k.z * k.z + k.w * k.w;
+  float qk = q.x * k.x + q.y * k.y + q.z * k.z + q.w * k.w;
+  qq = warp_sum(qq);
+  kk = warp_sum(kk);
+  qk = warp_sum(qk);
+  const float rq = rsqrtf(qq + kL2Eps);
+  const float rk = rsqrtf(kk + kL2Eps);
+  const float4 kh = make_float4(k.x * rk, k.y * rk, k.z * rk, k.w * rk);
+  const float4 qh = make_float4(q.x * rq, q.y * rq, q.z * rq, q.w * rq);
+  float4* ab = reinterpret_cast<float4*>(cab + 4 * lane);
+  float4* dk = reinterpret_cast<float4*>(cdk + 4 * lane);
+  ab[0] = make_float4(d.x * kh.x, d.x * qh.x, d.y * kh.y, d.y * qh.y);
+  ab[1] = make_float4(d.z * kh.z, d.z * qh.z, d.w * kh.w, d.w * qh.w);
+  dk[0] = make_float4(d.x, kh.x, d.y, kh.y);
+  dk[1] = make_float4(d.z, kh.z, d.w, kh.w);
+  return qk * rq * rk;
+}
+
+// Logistic function from the hardware exponential and an approximate
+// reciprocal: 1 / (1 + e^-x), within a few float32 ulps of the rounded
+// value; gives 0 where e^-x overflows.
+__device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
+
 }  // namespace
 
 // =====================================================================================
@@ -43,7 +72,9 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // clusters): warp w owns key rows [16w, 16w+16) of all W columns and the
 // warps' partial reductions meet in shared memory, one CTA barrier per
 // token; every CTA keeps 8 warps for the conv and coefficient phases while
-// each SM stores only W/128 of the state.  The state slab is loaded once from the start slot (the
+// each SM stores only W/128 of the state.  The per-row coefficients a
+// token's reduction reads, (d k_hat, d q_hat), and those its update reads,
+// (d, k_hat), sit in two arrays of pairs: one 8-byte shared load each.  The state slab is loaded once from the start slot (the
 // checkpoint of the last accepted token) and carried in float32 registers
 // across the sequence's tokens; after each token it is stored to that
 // token's checkpoint slot (rounded once if bf16), so a call moves one state
@@ -59,17 +90,19 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // lookup; then the state slab and the conv history are loaded.
 //
 // Tokens go in chunks of up to TC:
-//  A. conv + SiLU of the chunk's tokens for the CTA's 256 + W channels (each
-//     thread carries the raw history of its channels; a CTA writes the conv
-//     checkpoints of its slab of each section, so every channel is written
-//     once per cluster);
+//  A. conv + SiLU of the chunk's tokens for the CTA's 256 + W channels (the
+//     tokens of a channel are independent given its raw inputs; a CTA writes
+//     the conv checkpoints of its slab of each section, so every channel is
+//     written once per cluster);
 //  B. the warps normalise q, k of the chunk's tokens, form the decays and
 //     write the per-row coefficients (all 128 key rows, in every CTA);
-//  C. every warp runs the chunk's tokens on its strip with no CTA barrier:
-//     reduction, update, checkpoint store, raw output and its sum of squares;
-//  D. the RMSNorm sum of squares is combined over the cluster through
-//     distributed shared memory, and each CTA writes its slab of the gated
-//     outputs.
+//  C. every warp runs the chunk's tokens on its strip (column form: no CTA
+//     barrier): reduction, update, checkpoint store, raw output.  Nothing
+//     else rides on this sequential chain;
+//  D. one warp per token sums the squares of the slab's raw outputs and
+//     writes the sum into every CTA of the cluster (distributed shared
+//     memory); after one cluster barrier each CTA adds the CL sums locally
+//     and writes its slab of the gated outputs.
 // Grid slice n == N zeroes the padding token rows outside [qsl[0], qsl[N]).
 // =====================================================================================
 template <typename StateT, int W, int NW, bool ROWSPLIT>
@@ -97,11 +130,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   __shared__ __align__(16) __nv_bfloat16 s_gr[TC][kD];  // staged raw gates
   __shared__ __align__(16) __nv_bfloat16 s_og[TC][W];   // staged output-gate logits (slab)
   __shared__ __align__(16) float s_act[TC][NCH];        // SiLU(conv)
-  __shared__ float4 s_coef[TC][kD];                     // (d k_hat, d q_hat, d, k_hat) per key row
+  __shared__ __align__(16) float2 s_cab[TC][kD];        // (d k_hat, d q_hat) per key row
+  __shared__ __align__(16) float2 s_cdk[TC][kD];        // (d, k_hat) per key row
   __shared__ float2 s_tok[TC];                          // (beta, q_hat . k_hat)
   __shared__ int s_slot[TC];                            // checkpoint slot, 0 = none
-  __shared__ float s_ss[TC][NW];                        // per-warp sums of squares
-  __shared__ float s_part[TC];                          // this CTA's sum of squares per token
+  __shared__ float s_part[2][CL][TC];                   // CTA r's sum of squares per token (2 chunk buffers)
   __shared__ __nv_bfloat16 s_hist[3][NCH];              // raw conv history, oldest first (thread-owned)
   __shared__ float2 s_red[ROWSPLIT ? 2 : 1][ROWSPLIT ? NW : 1][ROWSPLIT ? W : 1];  // row form: (a, b) partials
 
@@ -122,6 +155,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   // Persistent: each cluster walks the units (sequence, head) with a stride
   // of the grid's cluster count; the padding slice is unit N*H .. (N+1)*H-1.
   const int num_units = (a.N + 1) * a.H;
+  int chunk = 0;  // chunks this CTA has run, across its units: selects the sum-of-squares buffer
   const int unit_stride = gridDim.x / CL;
   for (int unit = blockIdx.x / CL; unit < num_units; unit += unit_stride) {
   const int h = unit % a.H;
@@ -254,33 +288,49 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     if (tid == 0 && tc0 == t0 && next_n < a.N && pf_t1 > pf_t0 && pf_acc >= 1 && pf_acc <= a.cols)
       pf_slot = __ldg(a.idx + (int64_t)next_n * a.idx_rs + pf_acc - 1);
     // ---- A: conv + SiLU and this CTA's share of the conv checkpoints
+    // The raw inputs of a channel, oldest first: its three history taps, then
+    // the chunk's tokens.  Token j's conv reads entries j .. j+3 and leaves
+    // the history j+1 .. j+3, so the chunk's tokens are independent here.
     for (int lc = tid; lc < NCH; lc += NT) {
       const int sec = sec_of(lc), cis = cis_of(lc);
       const int64_t ch = (int64_t)sec * HD + h * kD + cis;
       const bool owner = cis >= slab0 && cis < slab0 + W;
       const float w0 = s_w[0][lc], w1 = s_w[1][lc], w2 = s_w[2][lc], w3 = s_w[3][lc];
-      __nv_bfloat16 h0 = s_hist[0][lc], h1 = s_hist[1][lc], h2 = s_hist[2][lc];
-      for (int j = 0; j < nt; ++j) {
-        const __nv_bfloat16 xn = s_x[j][lc];
-        float y = w0 * __bfloat162float(h0);
-        y = fmaf(w1, __bfloat162float(h1), y);
-        y = fmaf(w2, __bfloat162float(h2), y);
-        y = fmaf(w3, __bfloat162float(xn), y);
-        s_act[j][lc] = y * sigmoidf_(y);
-        h0 = h1;
-        h1 = h2;
-        h2 = xn;
-        const int sl = s_slot[j];
-        if (owner && sl != 0) {
-          __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + ch;
-          cp[0] = h0;
-          cp[a.cs_tap_stride] = h1;
-          cp[2 * a.cs_tap_stride] = h2;
+      __nv_bfloat16 xr[TC + 3];
+#pragma unroll
+      for (int p = 0; p < 3; ++p) xr[p] = s_hist[p][lc];
+#pragma unroll
+      for (int j = 0; j < TC; ++j) xr[3 + j] = j < nt ? s_x[j][lc] : __float2bfloat16(0.f);
+#pragma unroll
+      for (int j = 0; j < TC; ++j) {
+        if (j < nt) {
+          float y = w0 * __bfloat162float(xr[j]);
+          y = fmaf(w1, __bfloat162float(xr[j + 1]), y);
+          y = fmaf(w2, __bfloat162float(xr[j + 2]), y);
+          y = fmaf(w3, __bfloat162float(xr[j + 3]), y);
+          s_act[j][lc] = y * sigmoid_fast(y);
         }
       }
-      s_hist[0][lc] = h0;
-      s_hist[1][lc] = h1;
-      s_hist[2][lc] = h2;
+      if (owner) {
+#pragma unroll
+        for (int j = 0; j < TC; ++j) {
+          const int sl = j < nt ? s_slot[j] : 0;
+          if (sl != 0) {
+            __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + ch;
+            cp[0] = xr[j + 1];
+            cp[a.cs_tap_stride] = xr[j + 2];
+            cp[2 * a.cs_tap_stride] = xr[j + 3];
+          }
+        }
+      }
+#pragma unroll
+      for (int p = 0; p < 3; ++p) {
+        __nv_bfloat16 hv = xr[p];
+#pragma unroll
+        for (int q = 1; q <= TC; ++q)
+          if (q == nt) hv = xr[q + p];
+        s_hist[p][lc] = hv;
+      }
     }
     if (tid == 0 && tc0 == t0)
       s_pf = make_int4(pf_slot > 0 && pf_slot < a.num_slots ? pf_slot : 0, pf_t0, min(pf_t1, pf_t0 + TC),
@@ -325,7 +375,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
                                    expf(log_decay(bf_hi(gr.x) + dtb.y, A, a.gate_mode, a.lower_bound)),
                                    expf(log_decay(bf_lo(gr.y) + dtb.z, A, a.gate_mode, a.lower_bound)),
                                    expf(log_decay(bf_hi(gr.y) + dtb.w, A, a.gate_mode, a.lower_bound)));
-      const float qk = token_coefficients(q, k, d, lane, s_coef[j]);
+      const float qk = token_coefficient_pairs(q, k, d, lane, s_cab[j], s_cdk[j]);
       if (lane == 0) s_tok[j].y = qk;
     }
     __syncthreads();
@@ -333,12 +383,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     // ---- C: the chunk's tokens on this warp's fragments
     for (int j = 0; j < nt; ++j) {
       const float2 tk = s_tok[j];
-      const float4* coef = s_coef[j];
       float2 a2[G::VEC / 2], b2[G::VEC / 2];
 #pragma unroll
       for (int q = 0; q < G::VEC / 2; ++q) { a2[q] = make_float2(0.f, 0.f); b2[q] = make_float2(0.f, 0.f); }
 #pragma unroll
-      for (int i = 0; i < P; ++i) accumulate_row<G::VEC / 2>(coef[row0 + i * G::RPI], S[i], a2, b2);
+      for (int i = 0; i < P; ++i) {
+        const float2 c = s_cab[j][row0 + i * G::RPI];
+        accumulate_row<G::VEC / 2>(make_float4(c.x, c.y, 0.f, 0.f), S[i], a2, b2);
+      }
       float acc_a[G::VEC], acc_b[G::VEC];
       strip_allreduce<G>(a2, b2, acc_a, acc_b);
       if constexpr (ROWSPLIT) {  // combine the warps' row partials
@@ -361,19 +413,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
         }
       }
       float u[G::VEC], o[G::VEC];
-      float ss = 0.f;
 #pragma unroll
       for (int jj = 0; jj < G::VEC; ++jj) {
         u[jj] = tk.x * (s_act[j][2 * kD + lcol + jj] - acc_a[jj]);
         o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
-        ss = fmaf(o[jj], o[jj], ss);
       }
       float2 u2[G::VEC / 2];
       pairs_of<G::VEC>(u, u2);
 #pragma unroll
       for (int i = 0; i < P; ++i) {
-        const float4 c = coef[row0 + i * G::RPI];
-        update_row<G::VEC / 2>(c.z, c.w, S[i], u2, S[i]);
+        const float2 c = s_cdk[j][row0 + i * G::RPI];
+        update_row<G::VEC / 2>(c.x, c.y, S[i], u2, S[i]);
       }
       const int sl = s_slot[j];
       if (sl != 0) {
@@ -382,47 +432,48 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
         for (int i = 0; i < P; ++i) Frag<StateT>::store(sp + (row0 + i * G::RPI) * kD + col0, Frag<StateT>::pack2(S[i]));
       }
       // lanes of the first row of each strip hold distinct columns (row form: warp 0 only)
-      const bool writer = (lane < G::LPR) && (!ROWSPLIT || warp == 0);
-      if (writer) {
+      if (lane < G::LPR && (!ROWSPLIT || warp == 0)) {
 #pragma unroll
         for (int jj = 0; jj < G::VEC; ++jj) s_o[j][lcol + jj] = o[jj];
       }
-      ss = warp_sum(writer ? ss : 0.f);
-      if (lane == 0) s_ss[j][warp] = ss;
     }
     __syncthreads();
-    if (tid < nt) {
-      float p = 0.f;
+    // Sums of squares of the slab's raw outputs, one warp per token, sent to
+    // every CTA of the cluster (chunk buffers alternate, so a fast CTA's next
+    // chunk never overwrites sums a peer is still reading).
+    const int pb = chunk & 1;
+    for (int j = warp; j < nt; j += NW) {
+      float ss = 0.f;
 #pragma unroll
-      for (int w = 0; w < NW; ++w) p += s_ss[tid][w];
-      s_part[tid] = p;
+      for (int c = lane; c < W; c += 32) ss = fmaf(s_o[j][c], s_o[j][c], ss);
+      ss = warp_sum(ss);
+      if constexpr (CL > 1) {
+        if (lane < CL) *cg::this_cluster().map_shared_rank(&s_part[pb][rank][j], lane) = ss;
+      } else {
+        if (lane == 0) s_part[pb][0][j] = ss;
+      }
     }
     if constexpr (CL > 1) {
-      cg::this_cluster().sync();  // every CTA's partial sums are visible cluster-wide
+      cg::this_cluster().sync();  // every CTA's sums have arrived in every CTA
     } else {
       __syncthreads();
     }
+    ++chunk;
 
     // ---- D: gated RMSNorm of this slab of the outputs
     for (int i = tid; i < nt * (W / 4); i += NT) {
       const int j = i / (W / 4), c4 = 4 * (i % (W / 4));
       float tot = 0.f;
-      if constexpr (CL > 1) {
-        cg::cluster_group cl = cg::this_cluster();
 #pragma unroll
-        for (int r = 0; r < CL; ++r) tot += *cl.map_shared_rank(&s_part[j], r);
-      } else {
-        tot = s_part[j];
-      }
+      for (int r = 0; r < CL; ++r) tot += s_part[pb][r][j];
       const float rinv = rsqrtf(tot * (1.f / kD) + a.norm_eps);
       const float4 o4 = *reinterpret_cast<const float4*>(&s_o[j][c4]);
       const uint2 g2 = *reinterpret_cast<const uint2*>(&s_og[j][c4]);
       const float4 nw = *reinterpret_cast<const float4*>(&s_nw[c4]);
-      float y[4] = {o4.x * rinv * nw.x * sigmoidf_(bf_lo(g2.x)), o4.y * rinv * nw.y * sigmoidf_(bf_hi(g2.x)),
-                    o4.z * rinv * nw.z * sigmoidf_(bf_lo(g2.y)), o4.w * rinv * nw.w * sigmoidf_(bf_hi(g2.y))};
+      float y[4] = {o4.x * rinv * nw.x * sigmoid_fast(bf_lo(g2.x)), o4.y * rinv * nw.y * sigmoid_fast(bf_hi(g2.x)),
+                    o4.z * rinv * nw.z * sigmoid_fast(bf_lo(g2.y)), o4.w * rinv * nw.w * sigmoid_fast(bf_hi(g2.y))};
       store_out<4>(out + (int64_t)(tc0 + j) * a.o_rs + c4, y);
     }
-    if constexpr (CL > 1) cg::this_cluster().sync();  // peers are done reading this CTA's partial sums
   }
   }  // units
 }
