@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   constexpr int P = ROWSPLIT ? (kD / NW) / G::RPI : G::PASSES;
   static_assert(!ROWSPLIT || (kD / NW) % G::RPI == 0, "row form: a warp's rows must tile its passes");
   static_assert(CL * W == kD && (CL == 1 || CL == 2 || CL == 4 || CL == 8), "slabs must tile the 128 columns");
+  static_assert(TC == 8, "the conv phase reads the chunk's checkpoint slots as two int4");
   static_assert(W % 8 == 0, "slabs are staged in 16-byte pieces");
   // The staged conv input (read in phase A) and the raw outputs (written in
   // phase C) share one buffer.
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   __shared__ __align__(16) float2 s_cab[TC][kD];        // (d k_hat, d q_hat) per key row
   __shared__ __align__(16) float2 s_cdk[TC][kD];        // (d, k_hat) per key row
   __shared__ float2 s_tok[TC];                          // (beta, q_hat . k_hat)
-  __shared__ int s_slot[TC];                            // checkpoint slot, 0 = none
+  __shared__ __align__(16) int s_slot[TC];              // checkpoint slot, 0 = none
   __shared__ float s_part[2][CL][TC];                   // CTA r's sum of squares per token (2 chunk buffers)
   __shared__ __nv_bfloat16 s_hist[3][NCH];              // raw conv history, oldest first (thread-owned)
   __shared__ float2 s_red[ROWSPLIT ? 2 : 1][ROWSPLIT ? NW : 1][ROWSPLIT ? W : 1];  // row form: (a, b) partials
@@ -300,21 +301,26 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
 #pragma unroll
       for (int p = 0; p < 3; ++p) xr[p] = s_hist[p][lc];
 #pragma unroll
-      for (int j = 0; j < TC; ++j) xr[3 + j] = j < nt ? s_x[j][lc] : __float2bfloat16(0.f);
+      for (int j = 0; j < TC; ++j) {  // staged rows >= nt are stale: read as zero
+        const __nv_bfloat16 t = s_x[j][lc];
+        xr[3 + j] = j < nt ? t : __float2bfloat16(0.f);
+      }
+      // All TC rows are computed without branches; rows >= nt are never read.
 #pragma unroll
       for (int j = 0; j < TC; ++j) {
-        if (j < nt) {
-          float y = w0 * __bfloat162float(xr[j]);
-          y = fmaf(w1, __bfloat162float(xr[j + 1]), y);
-          y = fmaf(w2, __bfloat162float(xr[j + 2]), y);
-          y = fmaf(w3, __bfloat162float(xr[j + 3]), y);
-          s_act[j][lc] = y * sigmoid_fast(y);
-        }
+        float y = w0 * __bfloat162float(xr[j]);
+        y = fmaf(w1, __bfloat162float(xr[j + 1]), y);
+        y = fmaf(w2, __bfloat162float(xr[j + 2]), y);
+        y = fmaf(w3, __bfloat162float(xr[j + 3]), y);
+        s_act[j][lc] = y * sigmoid_fast(y);
       }
       if (owner) {
+        const int4 sa = *reinterpret_cast<const int4*>(&s_slot[0]);
+        const int4 sb = *reinterpret_cast<const int4*>(&s_slot[4]);
+        const int sls[TC] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
 #pragma unroll
         for (int j = 0; j < TC; ++j) {
-          const int sl = j < nt ? s_slot[j] : 0;
+          const int sl = j < nt ? sls[j] : 0;
           if (sl != 0) {
             __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + ch;
             cp[0] = xr[j + 1];
