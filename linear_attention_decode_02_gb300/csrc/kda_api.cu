@@ -286,15 +286,21 @@ bool rows_aligned16(const View& v) {
 }
 
 // Packed fused speculative decode: CTAs per (sequence, head) cluster.
-// Measured on GB300 (H=12/24, T=5, CUDA-graph replays after an L2 flush):
-// at one sequence of 12 heads the 8-CTA row form is fastest (13.9 vs
-// 15.9 us fp32: the checkpoint stores spread over 8x the SMs); from 8
-// sequences up one CTA per unit wins (the clustered forms repeat the conv and
-// coefficient phases in every CTA).
-int plan_cluster(int64_t units, int sms) { return 8 * units <= sms ? 8 : 1; }
+// A cluster spreads a unit's checkpoint stores over its SMs but repeats the
+// conv and coefficient phases in every CTA, so the widest cluster whose CTAs
+// all fit one per SM wins.  Measured on GB300 (T=5, CUDA-graph replays after
+// an L2 flush), fp32 state: H=12 N=1 12.5 us at 8 CTAs (15.6 at 1); H=12 N=2
+// and H=24 N=1 13.8 / 13.5 us at 4 (15.6 / 15.4 at 1); H=12 N=4 15.1 us at
+// 2 (16.5 at 1); from H=12 N=8 up one CTA per unit.  With a bf16 state the
+// 4-CTA row form is slower than 2 CTAs (H=12 N=1: 16.6 vs 14.5 us), so bf16
+// goes from 8 straight to 2 (H=12 N=2: 14.4 vs 14.9 us at 1).
+int plan_cluster(int64_t units, int state_dtype, int sms) {
+  if (8 * units <= sms) return 8;
+  if (state_dtype == KDA_F32 && 4 * units <= sms) return 4;
+  return 2 * units <= sms ? 2 : 1;
+}
 
 int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
-  (void)state_dtype;
   (void)t_max;
   const int forced = g_split_override.load();
   if (op == KDA_OP_FUSED) return 1;
@@ -304,7 +310,7 @@ int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   // the units at five or more per SM 4 slabs, fewer than half the SM count
   // 16 slabs, 8 in between.
   if (op == KDA_OP_SPEC) return 2;
-  if (op == KDA_OP_PACKED_FUSED) return plan_cluster(units, sms);
+  if (op == KDA_OP_PACKED_FUSED) return plan_cluster(units, state_dtype, sms);
   if (units >= 5LL * sms) return 4;
   return 2 * units <= sms ? 16 : 8;
 }

@@ -360,10 +360,18 @@ def test_packed_fused_contract(lib):
 
 
 def test_packed_fused_cluster_policy(lib):
-    # eight CTAs per unit up to an eighth of the SM count in units, one above
+    # the widest cluster whose CTAs fit one per SM: 8, then 4 (fp32 only), 2, 1
     assert binding.kda_plan_split(4, 12, 0, 1, 152) == 8
     assert binding.kda_plan_split(4, 19, 0, 1, 152) == 8
-    assert binding.kda_plan_split(4, 20, 0, 1, 152) == 1
+    assert binding.kda_plan_split(4, 19, 1, 1, 152) == 8
+    assert binding.kda_plan_split(4, 20, 0, 1, 152) == 4
+    assert binding.kda_plan_split(4, 38, 0, 1, 152) == 4
+    assert binding.kda_plan_split(4, 20, 1, 1, 152) == 2
+    assert binding.kda_plan_split(4, 39, 0, 1, 152) == 2
+    assert binding.kda_plan_split(4, 76, 0, 1, 152) == 2
+    assert binding.kda_plan_split(4, 76, 1, 1, 152) == 2
+    assert binding.kda_plan_split(4, 77, 0, 1, 152) == 1
+    assert binding.kda_plan_split(4, 77, 1, 1, 152) == 1
     assert binding.kda_plan_split(4, 96, 0, 1, 152) == 1
     assert binding.kda_plan_split(4, 1536, 1, 1, 152) == 1
     assert binding.kda_plan_schedule(4, 12, 0, 1, 152) == 1
