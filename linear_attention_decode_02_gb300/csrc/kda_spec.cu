@@ -29,7 +29,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
   constexpr int TC = 8;
   constexpr int NT = NW * 32;
   static_assert(SPLIT * CW * NW == kD, "split must tile the 128 value columns");
-  __shared__ float4 s_coef[TC][kD];  // staged (q, k, g), then (P k, P q, k / P, k / P)
+  // Per key row: staged (q, k) and g, then (P k, P q) and k / P; the reduction
+  // reads one 8-byte pair a row, the update one float.
+  __shared__ __align__(16) float2 s_ab[TC][kD];
+  __shared__ __align__(16) float s_ku[TC][kD];
   __shared__ float4 s_tok[TC];       // (beta, q.k, largest per-row decay, -)
   __shared__ float s_P[kD];          // P at the chunk end, per key row
   __shared__ __align__(16) float s_v[TC][kD];  // the chunk's value vectors
@@ -94,9 +97,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
       const float rq = rsqrtf(qq + kL2Eps), rk = rsqrtf(kk + kL2Eps);
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        s_coef[j][4 * lane + i] = make_float4(f4get(q, i) * rq, f4get(k, i) * rk, f4get(g, i), 0.f);
+      float4* ab = reinterpret_cast<float4*>(&s_ab[j][4 * lane]);
+      ab[0] = make_float4(q.x * rq, k.x * rk, q.y * rq, k.y * rk);
+      ab[1] = make_float4(q.z * rq, k.z * rk, q.w * rq, k.w * rk);
+      reinterpret_cast<float4*>(s_ku[j])[lane] = g;
       if (lane == 0) {
         const float braw = load1(a.beta, (int64_t)t * a.b_rs + (int64_t)h * a.b_hs, a.beta_dtype);
         s_tok[j] = make_float4(a.beta_is_logit ? sigmoidf_(braw) : braw, qk * rq * rk, gm, 0.f);
@@ -117,11 +121,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
     for (int r = threadIdx.x; r < kD; r += NT) {
       float Gs = 0.f, P = 1.f;
       for (int j = 0; j < ne; ++j) {
-        const float4 c = s_coef[j][r];  // (q, k, g, -)
-        Gs += c.z;
+        const float2 c = s_ab[j][r];  // (q, k)
+        Gs += s_ku[j][r];  // g
         P = expf(Gs);
         const float ku = c.y * expf(-Gs);
-        s_coef[j][r] = make_float4(P * c.y, P * c.x, ku, ku);
+        s_ab[j][r] = make_float2(P * c.y, P * c.x);
+        s_ku[j][r] = ku;
       }
       s_P[r] = P;
     }
@@ -133,7 +138,17 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
       for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = s_v[j][col0 + jj];
       const float4 tk = s_tok[j];
       float acc_a[G::VEC], acc_b[G::VEC];
-      strip_reduce<G>(S, s_coef[j], row0, acc_a, acc_b);
+      {
+        float2 a2[G::VEC / 2], b2[G::VEC / 2];
+#pragma unroll
+        for (int p = 0; p < G::VEC / 2; ++p) { a2[p] = make_float2(0.f, 0.f); b2[p] = make_float2(0.f, 0.f); }
+#pragma unroll
+        for (int i = 0; i < G::PASSES; ++i) {
+          const float2 c = s_ab[j][row0 + i * G::RPI];
+          accumulate_row<G::VEC / 2>(make_float4(c.x, c.y, 0.f, 0.f), S.s[i], a2, b2);
+        }
+        strip_allreduce<G>(a2, b2, acc_a, acc_b);
+      }
       float u[G::VEC], o[G::VEC];
 #pragma unroll
       for (int jj = 0; jj < G::VEC; ++jj) {
@@ -151,8 +166,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
       pairs_of<G::VEC>(u, u2);
 #pragma unroll
       for (int i = 0; i < G::PASSES; ++i) {
-        const float4 c = s_coef[j][row0 + i * G::RPI];
-        const float2 ku = make_float2(c.z, c.w);
+        const float2 ku = dup2(s_ku[j][row0 + i * G::RPI]);
 #pragma unroll
         for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = fma2(ku, u2[p], S.s[i][p]);
       }
