@@ -521,6 +521,7 @@ def e2e(wl, steps, warmup, barrier):
     ev_k = [torch.cuda.Event() for _ in range(nb)]
     ev_out = [torch.cuda.Event() for _ in range(nb)]
     base = dict(wl.d)
+    dmaps = [{**base, **{k: dv[b][k] for k in keys}} for b in range(nb)]
 
     def step(i):
         b = i % nb
@@ -530,7 +531,7 @@ def e2e(wl, steps, warmup, barrier):
         ev_in[b].record(s_in)
         comp.wait_event(ev_in[b])
         comp.wait_event(ev_out[b])  # the output buffer has been copied out
-        wl.d = {**base, **{k: dv[b][k] for k in keys}}
+        wl.d = dmaps[b]
         wl.out = outs[b]
         wl.call(dv[b]["__idx__"])
         ev_k[b].record(comp)

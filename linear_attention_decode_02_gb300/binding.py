@@ -116,8 +116,22 @@ def desc(t):
     return d
 
 
+# A descriptor depends only on the tensor's address, dtype, shape and
+# strides, and the library only reads it, so the per-call marshalling reuses
+# descriptors cached on exactly those (bounded; cleared when full).
+_DESC_CACHE = {}
+_DESC_CACHE_MAX = 1024
+
+
 def _ref(t):
-    return ctypes.byref(desc(t))
+    key = (t.data_ptr(), t.dtype, t.shape, t.stride())
+    d = _DESC_CACHE.get(key)
+    if d is None:
+        d = desc(t)
+        if len(_DESC_CACHE) >= _DESC_CACHE_MAX:
+            _DESC_CACHE.clear()
+        _DESC_CACHE[key] = d
+    return ctypes.byref(d)
 
 
 def _stream(t):

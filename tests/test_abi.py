@@ -89,6 +89,19 @@ def _recurrent_args(B=2, H=2, N=4, qkv=torch.bfloat16, state=torch.float32):
     return t
 
 
+def test_cached_descriptors_equal_fresh_ones():
+    # the marshalling cache is keyed on everything a descriptor holds
+    base = torch.zeros(6, 4, 128, dtype=torch.bfloat16)
+    views = [base, base[1:], base[:, ::2], base.transpose(0, 1), torch.zeros(3, dtype=torch.int32),
+             torch.zeros(2, 3, 128, 128), torch.zeros(0, 4, dtype=torch.float32)]
+    for _ in range(2):
+        for t in views:
+            assert bytes(binding._ref(t)._obj) == bytes(desc(t))
+    for i in range(binding._DESC_CACHE_MAX + 8):
+        binding._ref(torch.zeros(1 + i % 7, 3)[: 1 + i % 5])
+    assert len(binding._DESC_CACHE) <= binding._DESC_CACHE_MAX
+
+
 def _call_recurrent(lib, t, has_lb=0, lb=0.0, scale=0.088):
     names = ["q", "k", "v", "raw_gate", "raw_beta", "A_log", "dt_bias", "state_indices", "state", "out"]
     ds = [desc(t[n]) if isinstance(t[n], torch.Tensor) else t[n] for n in names]
