@@ -333,6 +333,35 @@ def test_packed_stream_schedule(stream_schedule, B):
     assert binding.kda_device_error() == 0
 
 
+@pytest.mark.parametrize("B", [8, 100])
+def test_packed_graph_replay_with_new_inputs(B):
+    """Captured once (split schedule at B=8, streaming at B=100); the replay
+    sees new activations and slot indices, null rows included."""
+    N = 512
+    c1 = synth.packed_case(B, num_slots=N, seed=40 + B)
+    d = P.to_device(c1)
+    out = torch.empty(B, 1, 12, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run_packed(d, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    fresh = P.dev(c1["state"])
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _run_packed(d, out=out)
+    c2 = synth.packed_case(B, num_slots=N, seed=41 + B, make_state=False)
+    for key in ("mixed_qkv", "raw_gate", "raw_beta", "state_indices"):
+        d[key].copy_(c2[key].cuda())
+    c2["state"], c2["A_log"], c2["dt_bias"] = c1["state"], c1["A_log"], c1["dt_bias"]
+    d["state"].copy_(fresh)
+    before = d["state"].clone()
+    out.fill_(7.0)
+    g.replay()
+    torch.cuda.synchronize()
+    _check_packed(c2, d, before, out)
+
+
 def test_schedule_policy_queries():
     assert binding.kda_plan_schedule(0, 16384, 0, 1, 152) == binding.SCHED_SPLIT
     assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == binding.SCHED_STREAM

@@ -119,6 +119,39 @@ def test_verify_outputs_equal_spec_decode():
     assert (out_v.float() - out_s.float()).abs().max().item() <= P.OUT_ATOL
 
 
+def test_verify_graph_replay_with_dynamic_cu_seqlens():
+    """Captured with every row active; replayed with new tokens and an empty
+    middle row: the outputs and caches follow the new metadata."""
+    H, t_cap = 6, 4
+    case = synth.spec_case(3, 2, seed=15, H=H, lengths=[2, 2, 2], num_slots=8)
+    case["state_indices"] = torch.tensor([1, 2, 3], dtype=torch.int32)
+    d = P.to_device(case)
+    corr, kg = _caches(8, H, t_cap)
+    out = torch.zeros(6, H, 128, dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        _run(d, 2, corr, kg, out=out)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        _run(d, 2, corr, kg, out=out)
+    c2 = synth.spec_case(3, 2, seed=16, H=H, lengths=[2, 2, 2], num_slots=8)
+    c2["state"] = case["state"]
+    c2["state_indices"] = case["state_indices"]
+    c2["cu_seqlens"] = torch.tensor([0, 2, 2, 4], dtype=torch.int32)
+    for key in ("q", "k", "v", "g", "beta", "cu_seqlens"):
+        d[key].copy_(c2[key].cuda())
+    corr.fill_(float("nan"))
+    kg.fill_(float("nan"))
+    out.fill_(3.0)
+    before = d["state"].clone()
+    g.replay()
+    torch.cuda.synchronize()
+    _check(c2, d, before, out, corr, kg, t_cap)
+    assert torch.count_nonzero(out[4:]) == 0  # token rows past cu_seqlens[N] are padding
+
+
 def test_verify_without_caches():
     case = synth.spec_case(5, 3, seed=14, H=3)
     d = P.to_device(case)
