@@ -206,6 +206,12 @@ def test_packed_contract(lib):
         assert _passes_validation(_call_packed(lib, t)), _msg(lib)
 
 
+def test_empty_packed_and_fused_batches_launch_nothing(lib):
+    # zero rows pass validation and return before any device query
+    assert _call_packed(lib, _packed_args(B=0)) == OK, _msg(lib)
+    assert _call_fused(lib, _fused_args(rows=0)) == OK, _msg(lib)
+
+
 def _fused_args(H=8, rows=4, N=9, state=torch.float32):
     HD = H * 128
     return dict(x=torch.zeros(rows, 3 * HD, dtype=torch.bfloat16), conv_weight=torch.zeros(3, 4, HD),
@@ -332,6 +338,18 @@ def _call_pf(lib, t, eps=1e-5):
                                        d["A_log"], d["dt_bias"], d["state_indices"], d["query_start_loc"],
                                        d["num_accepted_tokens"], d["state"], d["output_gate"], d["norm_weight"],
                                        1, -5.0, eps, d["out"], None)
+
+
+def test_empty_token_rows_launch_nothing(lib):
+    # no token rows: the speculative and packed fused entry points return
+    # before any device query, whatever the sequence count
+    t = _spec_args(R=0, N=0)
+    t["cu_seqlens"] = torch.zeros(1, dtype=torch.int32)
+    t["state_indices"] = torch.zeros(0, dtype=torch.int32)
+    assert _call_spec(lib, t) == OK, _msg(lib)
+    t = _pf_args(R=0, N=2)
+    t["query_start_loc"] = torch.zeros(3, dtype=torch.int32)
+    assert _call_pf(lib, t) == OK, _msg(lib)
 
 
 def test_packed_fused_contract(lib):
