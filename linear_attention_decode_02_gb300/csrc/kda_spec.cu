@@ -22,6 +22,39 @@ namespace kda {
 constexpr float kSpecMaxLogDecay = 80.f;   // chunk bound on the summed per-token decay
 constexpr float kSpecLogDecayFloor = -60.f;
 
+// Column sums of a 16-column strip's two k-reductions by reduce-scatter over
+// the strip's 2 VEC row groups: at each level a lane keeps one half of its
+// values and adds its partner's copy of that half, so the lane of row group
+// rg ends holding value rg of (a_0 .. a_{VEC-1}, b_0 .. b_{VEC-1}) summed
+// over all rows.
+template <typename G>
+__device__ __forceinline__ float spec_reduce_scatter(const float2 (&a2)[G::VEC / 2], const float2 (&b2)[G::VEC / 2],
+                                                     int rg) {
+  constexpr int NV = 2 * G::VEC;
+  static_assert(NV == G::RPI, "one value per row group");
+  constexpr int LEVELS = NV == 8 ? 3 : (NV == 16 ? 4 : 0);
+  static_assert(LEVELS > 0, "8 or 16 row groups");
+  float v[NV];
+#pragma unroll
+  for (int p = 0; p < G::VEC / 2; ++p) {
+    v[2 * p] = a2[p].x; v[2 * p + 1] = a2[p].y;
+    v[G::VEC + 2 * p] = b2[p].x; v[G::VEC + 2 * p + 1] = b2[p].y;
+  }
+#pragma unroll
+  for (int l = 0; l < LEVELS; ++l) {
+    const int half = NV >> (l + 1);
+    const int bit = LEVELS - 1 - l;  // the row-group bit of this level, most significant first
+    const bool hi = (rg >> bit) & 1;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = hi ? v[i] : v[i + half];
+      const float keep = hi ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, G::LPR << bit);
+    }
+  }
+  return v[0];
+}
+
 template <typename StateT, int CW, int NW, bool VERIFY>
 __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel(const SpecArgs a) {
   using G = Strip<StateT, CW>;
@@ -133,11 +166,12 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
     __syncthreads();
     for (int j = 0; j < ne; ++j) {
       const int t = tc0 + j;
-      float vv[G::VEC];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = s_v[j][col0 + jj];
       const float4 tk = s_tok[j];
-      float acc_a[G::VEC], acc_b[G::VEC];
+      // bf16 state (16 row groups): the column sums by reduce-scatter, 24
+      // shuffles instead of 64; the lane of row group rg < VEC forms u for
+      // column rg, the lane VEC groups up forms o for it, every lane gathers u
+      constexpr bool kScatter = sizeof(StateT) == 2 && 2 * G::VEC == G::RPI;
+      float u[G::VEC], o[G::VEC];
       {
         float2 a2[G::VEC / 2], b2[G::VEC / 2];
 #pragma unroll
@@ -147,13 +181,22 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
           const float2 c = s_ab[j][row0 + i * G::RPI];
           accumulate_row<G::VEC / 2>(make_float4(c.x, c.y, 0.f, 0.f), S.s[i], a2, b2);
         }
-        strip_allreduce<G>(a2, b2, acc_a, acc_b);
-      }
-      float u[G::VEC], o[G::VEC];
+        if constexpr (kScatter) {
+          const float tot = spec_reduce_scatter<G>(a2, b2, row0);
+          const float uc = row0 < G::VEC ? tk.x * (s_v[j][col0 + row0] - tot) : 0.f;
+          const float u_lo = __shfl_xor_sync(0xffffffffu, uc, G::LPR * G::VEC);
+          if (row0 >= G::VEC) out[t * out_rs + row0 - G::VEC] = __float2bfloat16_rn(a.scale * (tot + tk.y * u_lo));
 #pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) {
-        u[jj] = tk.x * (vv[jj] - acc_a[jj]);
-        o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
+          for (int c = 0; c < G::VEC; ++c) u[c] = __shfl_sync(0xffffffffu, uc, c * G::LPR + lane % G::LPR);
+        } else {
+          float acc_a[G::VEC], acc_b[G::VEC];
+          strip_allreduce<G>(a2, b2, acc_a, acc_b);
+#pragma unroll
+          for (int jj = 0; jj < G::VEC; ++jj) {
+            u[jj] = tk.x * (s_v[j][col0 + jj] - acc_a[jj]);
+            o[jj] = a.scale * (acc_b[jj] + tk.y * u[jj]);
+          }
+        }
       }
       if (VERIFY && a.corr != nullptr && row0 == 0 && t - t0 < a.t_cap) {
         float* cp = a.corr + (((int64_t)slot * a.H + h) * a.t_cap + (t - t0)) * kD + col0;
@@ -170,7 +213,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
 #pragma unroll
         for (int p = 0; p < G::VEC / 2; ++p) S.s[i][p] = fma2(ku, u2[p], S.s[i][p]);
       }
-      if (row0 == 0) store_out<G::VEC>(out + t * out_rs, o);
+      if (!kScatter && row0 == 0) store_out<G::VEC>(out + t * out_rs, o);
     }
     // restore the true state: S = P_end S~
 #pragma unroll
