@@ -54,6 +54,11 @@ MUTATIONS = {
     "softplus_gate_no_bias": ("gate_softplus", lambda r, d, a: ORIG_GATE_SP(r, np.zeros_like(d), a)),
     "bounded_gate_flipped": ("gate_lower_bound",
                              lambda r, d, a, lb: float(lb) - ORIG_GATE_LB(r, d, a, lb)),
+    "bounded_gate_no_A": ("gate_lower_bound", lambda r, d, a, lb: ORIG_GATE_LB(r, d, np.zeros_like(a), lb)),
+    "bounded_gate_A_not_exp": ("gate_lower_bound",
+                               lambda r, d, a, lb: float(lb) * ko.sigmoid(
+                                   np.asarray(a, np.float64)[..., :, None] *
+                                   (np.asarray(r, np.float64) + np.asarray(d, np.float64)))),
     "l2_eps_outside": ("l2_normalize",
                        lambda x, eps=ko.L2_EPS: np.asarray(x, np.float64) /
                        (np.sqrt(np.sum(np.asarray(x, np.float64) ** 2, -1, keepdims=True)) + 1e-2)),

@@ -105,6 +105,30 @@ def test_lower_bound_gate_identities():
     np.testing.assert_array_equal(ko.gate(raw, dt, A_log, None), ko.gate_softplus(raw, dt, A_log))
 
 
+def test_lower_bound_gate_per_head_rate():
+    # exp(A_log[h]) is a per-head rate on the pre-activation: head h's gate at
+    # x equals the unit-rate gate (A_log = 0) at exp(A_log[h]) * x
+    rng = _rng(31)
+    lb = -5.0
+    A_log = np.array([-2.0, -0.7, 0.0, 0.9])
+    H = A_log.size
+    raw = 2 * rng.standard_normal((H, 128))
+    dt = 0.1 * rng.standard_normal((H, 128))
+    g = ko.gate_lower_bound(raw, dt, A_log, lb)
+    x = raw + dt
+    unit = ko.gate_lower_bound(np.exp(A_log)[:, None] * x, np.zeros_like(x), np.zeros(H), lb)
+    np.testing.assert_allclose(g, unit, rtol=1e-13, atol=1e-15)
+    # heads with different rates differ away from the midpoint
+    assert np.abs(g[0] - ko.gate_lower_bound(raw[:1], dt[:1], A_log[1:2], lb)[0]).max() > 1e-3
+    # slope at the midpoint: d/dx lb * sigmoid(a x) at x = 0 is lb * a / 4
+    h = 1e-5
+    xs = np.array([[h], [-h]])
+    for hh in range(H):
+        gp, gm = ko.gate_lower_bound(xs, np.zeros_like(xs), np.full(2, A_log[hh]), lb)[:, 0]
+        slope = (gp - gm) / (2 * h)
+        np.testing.assert_allclose(slope, lb * np.exp(A_log[hh]) / 4, rtol=1e-8)
+
+
 def test_bf16_ulp_matches_torch_spacing():
     x = torch.tensor([1.0, 1.5, 3.0, 0.01, -7.25, 1e-3, 100.0], dtype=torch.bfloat16)
     nxt = (x.view(torch.int16) + 1).view(torch.bfloat16)
