@@ -30,6 +30,12 @@ __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
+// Split cluster barrier: arrive (release: this thread's earlier memory
+// accesses are ordered before the peers' accesses after their wait), then
+// wait (acquire).  Every thread of every CTA of the cluster must arrive once
+// before any of them can pass its wait.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
@@ -302,6 +308,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
 #pragma unroll
     for (int p = 0; p < 3; ++p) s_hist[p][lc] = cp[p * a.cs_tap_stride];
   }
+  // Cluster: every CTA reads the start slot's history of all q and k
+  // channels, but writes the checkpoints of its own slab only, and a
+  // checkpoint slot may be the start slot itself.  This arrive, with the wait
+  // before the first checkpoint store, orders every CTA's history reads
+  // before any peer's stores; it also guarantees that every CTA of the
+  // cluster is running before the first distributed-shared-memory store.
+  if constexpr (CL > 1) cluster_arrive();
 
   for (int tc0 = t0; tc0 < t1; tc0 += TC) {
     const int nt = min(TC, t1 - tc0);
@@ -324,6 +337,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
 
     if (tid == 0 && tc0 == t0 && next_n < a.N && pf_t1 > pf_t0 && pf_acc >= 1 && pf_acc <= a.cols)
       pf_slot = __ldg(a.idx + (int64_t)next_n * a.idx_rs + pf_acc - 1);
+    if constexpr (CL > 1) {
+      if (tc0 == t0) cluster_wait();  // every peer has read the start slot's conv history
+    }
     // ---- A: conv + SiLU and this CTA's share of the conv checkpoints
     // The raw inputs of a channel, oldest first: its three history taps, then
     // the chunk's tokens.  Token j's conv reads entries j .. j+3 and leaves

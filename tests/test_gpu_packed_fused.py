@@ -264,3 +264,31 @@ def test_packed_fused_every_start_slot_null():
     torch.cuda.synchronize()
     assert torch.count_nonzero(out) == 0
     assert torch.equal(st0, d["state"]) and torch.equal(cs0, d["conv_state"])
+
+
+@pytest.mark.parametrize("cluster", [2, 4, 8])
+def test_packed_fused_cluster_start_slot_is_first_checkpoint_repeated(cluster):
+    """With one accepted token the start slot is also the first checkpoint
+    slot, so each CTA of a cluster must read the slot's conv history before
+    any peer overwrites it with its slab's checkpoint.  Fifty repeated calls
+    from the same caches must give the oracle's result bit for bit every
+    time."""
+    binding.kda_set_split_override(cluster)
+    try:
+        case = synth.packed_fused_case(6, 5, H=3, seed=90 + cluster, lengths=[5, 3, 5, 1, 4, 5], accepted=1)
+        d, st0, cs0 = _setup(case)
+        out = _run(d)
+        torch.cuda.synchronize()
+        _check(case, d, st0, cs0, out)
+        first = (out.clone(), d["state"].clone(), d["conv_state"].clone())
+        for _ in range(50):
+            d["state"].copy_(st0)
+            d["conv_state"].copy_(cs0)
+            out.fill_(0.0)
+            _run(d, out=out)
+            torch.cuda.synchronize()
+            assert torch.equal(out, first[0])
+            assert torch.equal(d["state"], first[1])
+            assert torch.equal(d["conv_state"], first[2])
+    finally:
+        binding.kda_set_split_override(0)
