@@ -401,6 +401,73 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside)}
 
 
+class NvmlSampler:
+    """SM clock and clock-event reasons polled through NVML (read-only queries)
+    every `period` seconds from a thread, so that even a timed region of a few
+    milliseconds holds samples.  Same summary as ClockSampler."""
+
+    REASONS = (("hw_slowdown", 0x8), ("hw_thermal_slowdown", 0x40), ("sw_thermal_slowdown", 0x20),
+               ("sw_power_cap", 0x4))
+
+    def __init__(self, device_index=0, period=0.002):
+        import ctypes
+        self.ct = ctypes
+        self.samples = []
+        self.period = period
+        self.stop_ev = threading.Event()
+        self.thread = None
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        uuid = ClockSampler._physical_id(device_index).encode()
+        if lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(uuid), ctypes.byref(self.dev)) != 0:
+            raise OSError("no NVML handle for " + uuid.decode())
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx)) == 0 else None
+
+    def _poll(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_ev.is_set():
+            ok = self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(clk)) == 0
+            ok = ok and self.reasons_fn(self.dev, ct.byref(rs)) == 0
+            if ok:
+                self.samples.append((time.time(), float(clk.value), int(rs.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+        time.sleep(0.05)
+
+    def stop(self):
+        self.stop_ev.set()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        rows = inside or self.samples
+        if not rows:
+            return None
+        reasons = sorted({n for (_, _, r) in rows for n, bit in self.REASONS if r & bit})
+        return {"sm_mhz": statistics.median(c for (_, c, _) in rows), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(rows), "samples_in_timed_region": len(inside),
+                "source": "nvml, every %.0f ms" % (self.period * 1e3)}
+
+
+def clock_sampler(device_index):
+    """NVML poller when the library loads, else nvidia-smi at 100 ms."""
+    try:
+        return NvmlSampler(device_index)
+    except (OSError, AttributeError):
+        return ClockSampler(device_index)
+
+
 # ---- rank aggregation ------------------------------------------------------------------
 
 def reduce_max(x, dist=None, device="cpu"):
@@ -720,10 +787,21 @@ def main():
     peak_src = "measured" if peaks and peaks.get("hbm_gbs") else "fallback"
 
     wl = make_workload(args, seed=rank)
-    clocks = ClockSampler(torch.cuda.current_device())
+    clocks = clock_sampler(torch.cuda.current_device())
     clocks.start()
     ms, (w0, w1) = time_direct(wl.step, args.steps, args.warmup, barrier)
+    # Clock window: the same loop repeated for at least half a second, so
+    # that the clock record spans many samples as well; its time per step is
+    # reported beside the timed one (time x median clock can be compared).
+    reps = max(args.steps, int(math.ceil(0.5 / max(ms * 1e-3, 1e-6))))
+    ms_win, (v0, v1) = time_direct(wl.step, reps, 0, barrier)
     clocks.stop()
+    clock_rec = clocks.summary(w0, w1)
+    if clock_rec is not None:
+        win = clocks.summary(v0, v1)
+        clock_rec["window"] = {"steps": reps, "ms_per_step": round(ms_win, 5),
+                               "sm_mhz": win and win["sm_mhz"], "samples": win and win["samples_in_timed_region"],
+                               "reasons": win and win["reasons"]}
     ms_max = max_over_ranks(ms)
     value = job_gbs(wl.nbytes, world, ms_max)
     achieved = wl.nbytes / (ms * 1e-3) / 1e9
@@ -764,7 +842,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name), "kernel": name,
                          "peak_source": f"{peak_src} copy bandwidth (burst)"},
-            "e2e": e2e_obj, "clocks": clocks.summary(w0, w1), "cpu_baseline": cpu, "paths": paths,
+            "e2e": e2e_obj, "clocks": clock_rec, "cpu_baseline": cpu, "paths": paths,
             "kernel_source": source, "kernel_source_hash": kernel_source_hash(source),
         }
         print(json.dumps(line))

@@ -62,10 +62,7 @@ def test_fused_config_sweep(H, rows):
     before, cbefore = d["state"].clone(), d["conv_state"].clone()
     out = _run(d)
     torch.cuda.synchronize()
-    sample = None
-    if rows * H > 2048:
-        sample = sorted(np.random.default_rng(H).choice(rows, 16, replace=False).tolist())
-    _check(case, d, before, cbefore, out, rows=sample)
+    _check(case, d, before, cbefore, out)  # every row and slot
 
 
 @pytest.mark.parametrize("lower_bound", [-5.0, None])
@@ -143,8 +140,7 @@ def test_fused_stream_parity(stream_schedule, state_dtype, lower_bound, H, rows)
     out = torch.full((1, rows, H, 128), 7.0, dtype=torch.bfloat16, device="cuda")
     _run(d, lower_bound=lower_bound, out=out)
     torch.cuda.synchronize()
-    sample = None if rows * H <= 1024 else sorted(np.random.default_rng(3).choice(rows, 24, replace=False).tolist())
-    _check(case, d, before, cbefore, out, rows=sample, lower_bound=lower_bound)
+    _check(case, d, before, cbefore, out, lower_bound=lower_bound)
     assert binding.kda_device_error() == 0
 
 
@@ -171,8 +167,7 @@ def test_fused_stream_many_units_and_graph(stream_schedule):
     before, cbefore = d["state"].clone(), d["conv_state"].clone()
     g.replay()
     torch.cuda.synchronize()
-    rows_s = sorted(np.random.default_rng(4).choice(rows, 40, replace=False).tolist())
-    _check(c2, d, before, cbefore, out, rows=rows_s)
+    _check(c2, d, before, cbefore, out)
     assert binding.kda_device_error() == 0
 
 

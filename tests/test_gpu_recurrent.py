@@ -78,8 +78,7 @@ def test_kimi_linear_full_pool(B):
     before = d["state"].clone()
     out = _run_recurrent(d)
     torch.cuda.synchronize()
-    rows = None if B <= 128 else sorted(np.random.default_rng(0).choice(B, 48, replace=False).tolist())
-    _check_recurrent(case, d, before, out, rows=rows)
+    _check_recurrent(case, d, before, out)  # every row and slot against the oracle
 
 
 def test_strided_views_into_one_projection_row():
@@ -194,8 +193,7 @@ def test_packed_batch_sweep(B):
     before = d["state"].clone()
     out = _run_packed(d)
     torch.cuda.synchronize()
-    rows = None if B <= 128 else sorted(np.random.default_rng(1).choice(B, 64, replace=False).tolist())
-    _check_packed(case, d, before, out, rows=rows)
+    _check_packed(case, d, before, out)  # every row and slot against the oracle
 
 
 @pytest.mark.parametrize("split", SPLITS)
@@ -242,6 +240,38 @@ def test_packed_long_run_drift_stays_bounded():
     assert worst <= P.OUT_ATOL
 
 
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_long_run_drift_512_steps(state_dtype):
+    """Drift diagnostic: 512 chained T=1 steps on the same slots (H=4, 4 rows,
+    fresh activations every step), the GPU state carried in the pool's dtype
+    against the oracle carried in float64.  The curve (max abs error of the
+    outputs and of the state at steps 1, 2, 4, ..., 512) is reported in the
+    test session's summary; the gate only catches a blow-up."""
+    from oracle import kda_oracle as ko
+    B, H, M = 4, 4, 8
+    case = synth.recurrent_case(B, H, M, seed=13, state_dtype=state_dtype, null_count=0)
+    d = P.to_device(case)
+    idx = case["state_indices"].numpy()
+    pool = P.f64(case["state"])
+    curve = []
+    for step in range(1, 513):
+        sc = synth.recurrent_case(B, H, M, seed=1000 + step, state_dtype=state_dtype, null_count=0)
+        for key in ("q", "k", "v", "raw_gate", "raw_beta"):
+            d[key].copy_(sc[key].cuda())
+        out = _run_recurrent(d)
+        ref_out, pool = ko.recurrent_decode(P.f64(sc["q"]), P.f64(sc["k"]), P.f64(sc["v"]), P.f64(sc["raw_gate"]),
+                                            P.f64(sc["raw_beta"]), P.f64(case["A_log"]), P.f64(case["dt_bias"]),
+                                            idx, pool)
+        if step & (step - 1) == 0:
+            torch.cuda.synchronize()
+            e_out = float(np.abs(out.double().cpu().numpy() - ref_out).max())
+            e_st = float(np.abs(d["state"].double().cpu().numpy()[idx] - pool[idx]).max())
+            curve.append((step, e_out, e_st))
+    P.DRIFT[f"recurrent H=4 {str(state_dtype).split('.')[-1]} state"] = curve
+    assert all(np.isfinite(e) for _, a, b in curve for e in (a, b))
+    assert max(a for _, a, _ in curve) <= 10 * P.OUT_ATOL
+
+
 # ---- persistent streaming schedule (bulk copies into shared-memory stages) -----------
 
 @pytest.fixture
@@ -273,8 +303,7 @@ def test_stream_many_units_per_cta(stream_schedule, state_dtype):
     before = d["state"].clone()
     out = _run_recurrent(d)
     torch.cuda.synchronize()
-    rows = sorted(np.random.default_rng(2).choice(300, 60, replace=False).tolist())
-    _check_recurrent(case, d, before, out, rows=rows)
+    _check_recurrent(case, d, before, out)
     assert binding.kda_device_error() == 0
 
 
