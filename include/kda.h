@@ -290,23 +290,41 @@ kda_status kda_set_split_override(int32_t split);
  * shared-memory stages with bulk asynchronous copies while consumer warps
  * update earlier ones; needs every activation head vector (and, fused, the
  * conv-cache slots) 16-byte aligned, otherwise the call uses SPLIT, or
- * returns KDA_ERR_UNSUPPORTED if STREAM is forced.  kda_spec_decode has the
- * split schedule only.
+ * returns KDA_ERR_UNSUPPORTED if STREAM is forced.
+ * MMA (kda_spec_decode and kda_spec_verify_decode with a bfloat16 state
+ * pool): the chunked form of the token loop on the tensor cores ([P1]
+ * "Frozen / speculative-verify mode" names the WY-parallel tensor-core form
+ * of these rows): per chunk of up to 8 tokens, S^T [P k | P q] and the
+ * rank-T update run as tcgen05 MMAs with float32 accumulators in tensor
+ * memory, bf16 high/low operand splits keeping them within ~2^-16 of
+ * float32; one persistent CTA per SM.  Forcing MMA with a float32 state
+ * returns KDA_ERR_UNSUPPORTED.  The speculative entry points otherwise use
+ * SPLIT (one CTA per row, head and value slab, the state in registers).
  */
-typedef enum kda_schedule { KDA_SCHED_AUTO = 0, KDA_SCHED_SPLIT = 1, KDA_SCHED_STREAM = 2 } kda_schedule;
+typedef enum kda_schedule {
+  KDA_SCHED_AUTO = 0,
+  KDA_SCHED_SPLIT = 1,
+  KDA_SCHED_STREAM = 2,
+  KDA_SCHED_MMA = 3
+} kda_schedule;
 
 /* Schedule the dispatcher picks (same arguments as kda_plan_split); 0 on invalid arguments. */
 int32_t kda_plan_schedule(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max,
                           int32_t sm_count);
 
-/* Force the schedule of later T=1 calls (KDA_SCHED_AUTO restores the policy). */
+/* Force the schedule of later calls (KDA_SCHED_AUTO restores the policy):
+ * SPLIT / STREAM apply to the T=1 entry points, SPLIT / MMA to the
+ * speculative ones; a schedule an entry point does not have is ignored
+ * there. */
 kda_status kda_set_schedule_override(int32_t schedule);
 
 /*
  * Device error word of the streaming kernels on the current device: bit 0 =
  * a wait for a filled stage timed out (2 s), bit 1 = a wait for a free stage
- * timed out, bit 2 = the kda_selftest_wait_timeout wait gave up (expected).  A kernel that times out records the bit and returns early, its
- * results for the affected units are undefined.  Synchronises the device;
+ * timed out, bit 2 = the kda_selftest_wait_timeout wait gave up (expected),
+ * bit 3 = a wait of the tensor-core (MMA) speculative kernel timed out.  A
+ * kernel that times out records the bit and returns early, its results for
+ * the affected units are undefined.  Synchronises the device;
  * clears the word when `clear` is non-zero.
  */
 kda_status kda_device_error(uint32_t* flags, int32_t clear);

@@ -35,7 +35,7 @@ EXPORTS = ("kda_recurrent_decode", "kda_packed_decode", "kda_fused_decode", "kda
            "kda_plan_split", "kda_set_split_override", "kda_plan_schedule", "kda_set_schedule_override",
            "kda_device_error", "kda_selftest_wait_timeout", "kda_status_string", "kda_last_error_message",
            "kda_version")
-SCHED_AUTO, SCHED_SPLIT, SCHED_STREAM = 0, 1, 2
+SCHED_AUTO, SCHED_SPLIT, SCHED_STREAM, SCHED_MMA = 0, 1, 2, 3
 
 
 class KdaError(RuntimeError):
@@ -255,7 +255,8 @@ def kda_plan_schedule(op, units, state_dtype, t_max, sm_count):
 
 
 def kda_set_schedule_override(schedule):
-    """Force the T=1 schedule (SCHED_SPLIT / SCHED_STREAM; SCHED_AUTO restores the policy)."""
+    """Force the schedule (SCHED_SPLIT / SCHED_STREAM for T=1, SCHED_SPLIT / SCHED_MMA for the
+    speculative entry points; SCHED_AUTO restores the policy)."""
     lib = library()
     _check(lib, lib.kda_set_schedule_override(int(schedule)))
 

@@ -268,9 +268,14 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
 //  - speculative rows: the split kernel.
 int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)t_max;
-  if (op == KDA_OP_SPEC || op == KDA_OP_PACKED_FUSED) return KDA_SCHED_SPLIT;
   const int forced = g_schedule_override.load();
-  if (forced != KDA_SCHED_AUTO) return forced;
+  if (op == KDA_OP_PACKED_FUSED) return KDA_SCHED_SPLIT;
+  if (op == KDA_OP_SPEC) {
+    if (forced == KDA_SCHED_SPLIT || forced == KDA_SCHED_MMA) return forced;
+    (void)units; (void)sms; (void)state_dtype;
+    return KDA_SCHED_SPLIT;
+  }
+  if (forced == KDA_SCHED_SPLIT || forced == KDA_SCHED_STREAM) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
   if (op == KDA_OP_FUSED) return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
   if (state_dtype == KDA_F32) return KDA_SCHED_SPLIT;
@@ -781,6 +786,12 @@ kda_status spec_common(const kda_tensor* q, const kda_tensor* k, const kda_tenso
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   DeviceInfo dev;
   KDA_TRY(current_device(st, &dev));
+  int sched = plan_schedule(KDA_OP_SPEC, N * H, S.dtype, t_max, dev.sms);
+  if (sched == KDA_SCHED_MMA && S.dtype != KDA_BF16) {
+    KDA_CHECK(g_schedule_override.load() != KDA_SCHED_MMA, KDA_ERR_UNSUPPORTED,
+              "the tensor-core (MMA) schedule takes a bfloat16 state pool");
+    sched = KDA_SCHED_SPLIT;
+  }
   const int split = plan_split(KDA_OP_SPEC, N * H, S.dtype, t_max, dev.sms);
   KDA_CHECK(kda::split_supported(split), KDA_ERR_INVALID_ARG, "split %d has no kernel", split);
   KDA_TRY(check_grid((N + 1) * H * split));
@@ -802,6 +813,7 @@ kda_status spec_common(const kda_tensor* q, const kda_tensor* k, const kda_tenso
   a.corr = verify && correction_cache != nullptr ? reinterpret_cast<float*>(CC.data) : nullptr;
   a.kg = verify && kg_cache != nullptr ? reinterpret_cast<float*>(KG.data) : nullptr;
   a.t_cap = (int32_t)t_cap;
+  if (sched == KDA_SCHED_MMA) return check_launch(kda::launch_spec_mma(a, verify, dev.sms, st));
   return check_launch(kda::launch_spec(a, S.dtype, split, verify, st));
 }
 
@@ -840,7 +852,8 @@ int32_t kda_plan_schedule(int32_t op, int64_t units, int32_t state_dtype, int32_
 }
 
 kda_status kda_set_schedule_override(int32_t schedule) {
-  KDA_CHECK(schedule == KDA_SCHED_AUTO || schedule == KDA_SCHED_SPLIT || schedule == KDA_SCHED_STREAM,
+  KDA_CHECK(schedule == KDA_SCHED_AUTO || schedule == KDA_SCHED_SPLIT || schedule == KDA_SCHED_STREAM ||
+                schedule == KDA_SCHED_MMA,
             KDA_ERR_INVALID_ARG, "unknown schedule %d", schedule);
   g_schedule_override.store(schedule);
   return KDA_OK;
@@ -848,10 +861,11 @@ kda_status kda_set_schedule_override(int32_t schedule) {
 
 kda_status kda_device_error(uint32_t* flags, int32_t clear) {
   KDA_CHECK(flags != nullptr, KDA_ERR_INVALID_ARG, "flags: null pointer");
-  unsigned int f = 0;
+  unsigned int f = 0, fm = 0;
   cudaError_t e = kda::read_device_error(&f, clear != 0);
+  if (e == cudaSuccess) e = kda::read_mma_error(&fm, clear != 0);
   KDA_CHECK(e == cudaSuccess, KDA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
-  *flags = f;
+  *flags = f | fm;
   return KDA_OK;
 }
 

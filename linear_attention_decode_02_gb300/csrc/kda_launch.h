@@ -80,6 +80,14 @@ cudaError_t launch_t1_stream(const T1Args& a, int state_dtype, int sm_count, cud
 // slots, raw-gate and output-gate head vectors.
 cudaError_t launch_fused_stream(const FusedArgs& a, int state_dtype, int sm_count, cudaStream_t s);
 
+// Speculative decode (and verify) in the chunked tensor-core form, bfloat16
+// state only: persistent, one CTA per SM (sized from `sm_count`).
+cudaError_t launch_spec_mma(const SpecArgs& a, bool verify, int sm_count, cudaStream_t s);
+
+// Reads (and optionally clears) the error word of the tensor-core
+// speculative kernel: bit 3 = one of its waits timed out.
+cudaError_t read_mma_error(unsigned int* flags, bool clear);
+
 // One warp waiting on a barrier nothing completes (bounded-wait self-test).
 cudaError_t launch_selftest_wait(cudaStream_t s);
 

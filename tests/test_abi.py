@@ -416,7 +416,11 @@ def test_schedule_override_and_plan(lib):
     assert lib.kda_set_schedule_override(7) == INVALID
     assert lib.kda_set_schedule_override(2) == OK
     assert binding.kda_plan_schedule(0, 1, 0, 1, 152) == 2
-    assert binding.kda_plan_schedule(3, 1, 0, 1, 152) == 1  # spec has one schedule
+    assert binding.kda_plan_schedule(3, 1, 0, 1, 152) == 1  # stream does not apply to spec rows
+    assert lib.kda_set_schedule_override(3) == OK  # tensor-core chunked form: spec rows only
+    assert binding.kda_plan_schedule(3, 2048, 1, 6, 152) == 3
+    assert binding.kda_plan_schedule(0, 16384, 1, 1, 152) == 2  # T=1 ignores it
+    assert binding.kda_plan_schedule(4, 12, 0, 1, 152) == 1
     assert lib.kda_set_schedule_override(0) == OK
     assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 2  # bf16 packed: stream
     assert binding.kda_plan_schedule(1, 12, 1, 1, 152) == 1
