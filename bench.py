@@ -211,10 +211,15 @@ class Fused(Workload):
 
 
 class Spec(Workload):
-    def __init__(self, N=128, t_max=6, H=16, slots=None, state_dtype=torch.float32, n_sets=2, seed=0):
+    """Ragged speculative rows (lengths 1..t_max, some empty), or with
+    `fixed` every row exactly t_max tokens long."""
+
+    def __init__(self, N=128, t_max=6, H=16, slots=None, state_dtype=torch.float32, n_sets=2, seed=0, fixed=False):
         slots = slots or 4 * N
-        self.name = f"spec_h{H}_n{N}_t{t_max}_{'f32' if state_dtype == torch.float32 else 'bf16'}"
-        c = synth.spec_case(N, t_max, seed=seed, H=H, num_slots=slots, make_state=False)
+        self.name = (f"spec_h{H}_n{N}_t{t_max}{'_fixed' if fixed else ''}_"
+                     f"{'f32' if state_dtype == torch.float32 else 'bf16'}")
+        c = synth.spec_case(N, t_max, seed=seed, H=H, num_slots=slots, make_state=False,
+                            lengths=[t_max] * N if fixed else None)
         self.t_max = t_max
         self.d = {k: v.cuda() for k, v in c.items() if isinstance(v, torch.Tensor) and k not in ("state",
                                                                                                    "state_indices")}
@@ -225,7 +230,8 @@ class Spec(Workload):
         lens = c["lengths"]
         live_rows = int((lens > 0).sum())
         self.nbytes = bytes_spec(R, live_rows, N, R, H, 4 if state_dtype == torch.float32 else 2)
-        self.config = dict(workload="packed_speculative_ragged", H=H, rows=N, t_max=t_max, tokens=R,
+        self.config = dict(workload="packed_speculative_" + ("fixed" if fixed else "ragged"), H=H, rows=N,
+                           t_max=t_max, tokens=R,
                            empty_rows=N - live_rows, num_slots=slots,
                            state="float32" if state_dtype == torch.float32 else "bfloat16",
                            gates="precomputed fp32 log decay in [-5, 0]")
@@ -628,10 +634,16 @@ def path_measurements(flush, peak):
     """CUDA-graph timings of the decode entry points over their configured sizes."""
     res = {}
 
-    def run(wl, n_sets):
-        ms = time_graph(wl, n_sets, 10, flush)
+    def run(wl, n_sets, schedule=None):
+        if schedule is not None:
+            binding.kda_set_schedule_override(schedule)
+        try:
+            ms = time_graph(wl, n_sets, 10, flush)
+        finally:
+            binding.kda_set_schedule_override(binding.SCHED_AUTO)
         gbs = wl.nbytes / (ms * 1e-3) / 1e9
-        res[wl.name] = dict(us=round(ms * 1e3, 3), gbs=round(gbs, 1), frac=round(gbs / peak, 4))
+        name = wl.name + ("_mma" if schedule == binding.SCHED_MMA else "")
+        res[name] = dict(us=round(ms * 1e3, 3), gbs=round(gbs, 1), frac=round(gbs / peak, 4))
 
     for B in (1, 8, 32, 128, 512):
         n = max(1, min(16, 1023 // B))
@@ -644,6 +656,11 @@ def path_measurements(flush, peak):
         run(Fused(H=H, rows=rows, n_sets=n, seed=H + rows), n)
     for N, T in ((1, 6), (16, 6), (128, 2), (128, 4), (128, 6)):
         run(Spec(N=N, t_max=T, H=16, n_sets=2, seed=N + T), 2)
+    # bf16 state: the per-token kernel (the policy's choice) and the tensor-core
+    # chunked form, on ragged rows and on rows of exactly T tokens
+    for N, T, fixed in ((128, 6, False), (128, 6, True), (128, 8, True), (128, 16, True)):
+        for sched in (None, binding.SCHED_MMA):
+            run(Spec(N=N, t_max=T, H=16, state_dtype=torch.bfloat16, n_sets=2, seed=N + T, fixed=fixed), 2, sched)
     for H, N in ((12, 1), (12, 8), (12, 32), (12, 128), (24, 8), (24, 128)):
         for dt in (torch.float32, torch.bfloat16):
             run(PackedFused(N=N, T=5, H=H, state_dtype=dt, n_sets=2, seed=H + N), 2)

@@ -22,12 +22,13 @@
 //   GEMM 2: [X](128 x nt) [u](nt x 128): M = 128 key rows, N = 128, K = 48
 //           holding the six piece products x_i u_j with i + j <= 4.
 // A float32 value is the sum of three bf16 pieces to within 2^-24 of itself,
-// so both products carry float32 accuracy; the accumulators are float32 in
-// tensor memory, and S' = P_end (S + GEMM 2) is formed in float32 and rounded
-// to bf16 once.  Rows longer than a chunk run chunk after chunk: between
-// chunks the float32 state is kept in tensor memory for the next epilogue,
-// and as a bf16 high part (in the stage) plus a bf16 low part for the next
-// GEMM 1.
+// so both products carry float32 accuracy.  GEMM 2 accumulates onto the
+// state itself: the accumulator (float32, tensor memory) is first seeded with
+// S by an MMA of the identity (held in tensor memory) and the TMA-loaded
+// tile, so the epilogue only scales each key row by P_end and rounds to bf16
+// once.  Rows longer than a chunk run chunk after chunk: between chunks the
+// float32 state stays in the accumulator, and a bf16 high part (in the stage)
+// plus a bf16 low part serve as the next GEMM 1's A operand.
 //
 // One persistent CTA per SM walks its units; warps are specialised:
 //   warp 0      TMA loads of state blocks into a ring of MS stages;
@@ -64,10 +65,10 @@ constexpr int EPI_WARP0 = 2 + NPRO;       // first epilogue warp
 constexpr int MMA_THREADS = (EPI_WARP0 + 4) * 32;
 constexpr float kMaxChunkDecay = 80.f;    // chunk bound on the summed largest per-token decay
 constexpr float kLogDecayFloor = -60.f;
-constexpr uint32_t TMEM_COLS = 512;       // D1 x 2 (64 columns each), D2 (128), carried state (128)
+constexpr uint32_t TMEM_COLS = 512;       // D1 x 2 (64 columns), state accumulator x 2 (128), identity (64)
 constexpr uint32_t D1_STRIDE = 64;
-constexpr uint32_t D2_COL = 128;
-constexpr uint32_t CARRY_COL = 256;
+constexpr uint32_t ACC_COL = 128;         // accumulator of unit parity p: ACC_COL + 128 p
+constexpr uint32_t IDENT_COL = 384;       // 128 x 128 bf16 identity (A operand), two per column
 constexpr int N1 = 6 * MT;                // GEMM 1 columns: [Y | Z] x three pieces
 
 constexpr uint32_t SZ_STATE = 32768;      // bf16 128 x 128
@@ -105,6 +106,8 @@ static_assert(O_LO % 1024 == 0 && O_W1 % 1024 == 0 && O_W2 % 1024 == 0 && O_U2 %
 // GEMM 1: M = 128 (A = state, MN-major), N = N1 (B K-major); GEMM 2: M = N = 128 (A MN-major, B K-major).
 constexpr uint32_t ID1 = tc::idesc_bf16(128, N1, true, false);
 constexpr uint32_t ID2 = tc::idesc_bf16(128, 128, true, false);
+// Seeding the accumulator with the state: I (A, in tensor memory) times S (B, MN-major).
+constexpr uint32_t IDS = tc::idesc_bf16(128, 128, false, true);
 
 __device__ __forceinline__ void record_mma_error() { atomicOr(&g_kda_mma_error, 8u); }
 
@@ -262,6 +265,20 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) kda_spec_mma_kernel(const Spec
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t taddr = *s_taddr;
+  if (warp >= EPI_WARP0) {  // the identity, once: lane k holds 1.0 (bf16 0x3F80) at K index k
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t one = (r & 1) ? 0x3F800000u : 0x00003F80u;
+#pragma unroll
+    for (int h32 = 0; h32 < 2; ++h32) {
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(32 * h32 + i == (r >> 1) ? one : 0u);
+      tc::st32(taddr + ((uint32_t)(32 * (warp & 3)) << 16) + IDENT_COL + 32 * h32, z);
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
 
   const int G = gridDim.x;
   const int n_my = (a.N * a.H - (int)blockIdx.x + G - 1) / G;  // units blockIdx.x + j * G
@@ -367,6 +384,11 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) kda_spec_mma_kernel(const Spec
               for (int ks = 0; ks < 8; ++ks)
                 tc::mma_bf16(d1, tc::desc_sw128(lo + ks * 2048, 16384, 1024),
                              tc::desc_sw128(w1 + (ks >> 2) * SZ_W1A + (ks & 3) * 32, 16, 1024), ID1, true);
+            } else if (!VERIFY || !last) {  // the unit's accumulator starts as S (exactly, in float32)
+#pragma unroll
+              for (int ks = 0; ks < 8; ++ks)
+                tc::mma_bf16_ta(taddr + ACC_COL + 128 * (L & 1), taddr + IDENT_COL + 8 * ks,
+                                tc::desc_sw128(st + ks * 2048, 16384, 1024), IDS, ks > 0);
             }
             tc::commit(&d1full[b]);
           }
@@ -379,9 +401,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) kda_spec_mma_kernel(const Spec
               tc::fence_after_sync();
               const uint32_t w2 = smem_addr(sm + O_W2 + b * SZ_W2), u2 = smem_addr(sm + O_U2);
 #pragma unroll
-              for (int ks = 0; ks < 3; ++ks)
-                tc::mma_bf16(taddr + D2_COL, tc::desc_sw128(w2 + ks * 2048, SZ_W1A, 1024),
-                             tc::desc_sw128(u2 + ks * 32, 16, 1024), ID2, ks > 0);
+              for (int ks = 0; ks < 3; ++ks)  // accumulator += X u^T
+                tc::mma_bf16(taddr + ACC_COL + 128 * (L & 1), tc::desc_sw128(w2 + ks * 2048, SZ_W1A, 1024),
+                             tc::desc_sw128(u2 + ks * 32, 16, 1024), ID2, true);
               tc::commit(d2full);
             }
             __syncwarp();
@@ -630,38 +652,21 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) kda_spec_mma_kernel(const Spec
             if (!wait_or_abort(d2full, g2 & 1)) { run = false; break; }
             ++g2;
             tc::fence_after_sync();
-            // ---- S' = P_end (S + GEMM 2): this thread is key row k = r
+            // ---- S' = P_end (S + X u^T), the accumulator scaled per key row: this thread is row k = r
             const float2 P2 = dup2(s_pend[b * kD + r]);
             unsigned char* lo = sm + O_LO;
+            const uint32_t acc = tl + ACC_COL + 128 * (L & 1);
 #pragma unroll 1
             for (int hb = 0; hb < 2; ++hb) {  // value columns 64 hb .. 64 hb + 63: stage block hb
               float d[64];
-              tc::ld64(tl + D2_COL + 64 * hb, d);
-              const uint32_t row = hb * 16384 + r * 128;
-              // d <- P_end (S + d), column pairs at a time
-              auto fma_pair = [&](int e, float2 x) {
-                const float2 y = mul2(P2, add2(x, make_float2(d[2 * e], d[2 * e + 1])));
+              tc::ld64(acc + 64 * hb, d);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const float2 y = mul2(P2, make_float2(d[2 * e], d[2 * e + 1]));
                 d[2 * e] = y.x;
                 d[2 * e + 1] = y.y;
-              };
-              if (c > 0) {  // the float32 state of the previous chunk, kept in tensor memory
-#pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                  float sc[32];
-                  tc::ld32(tl + CARRY_COL + 64 * hb + 32 * half, sc);
-#pragma unroll
-                  for (int e = 0; e < 16; ++e) fma_pair(16 * half + e, make_float2(sc[2 * e], sc[2 * e + 1]));
-                }
-              } else {
-#pragma unroll
-                for (int q8 = 0; q8 < 8; ++q8) {
-                  const uint4 sv = *reinterpret_cast<const uint4*>(st + row + ((q8 ^ (r & 7)) << 4));
-                  fma_pair(4 * q8 + 0, make_float2(bf_lo(sv.x), bf_hi(sv.x)));
-                  fma_pair(4 * q8 + 1, make_float2(bf_lo(sv.y), bf_hi(sv.y)));
-                  fma_pair(4 * q8 + 2, make_float2(bf_lo(sv.z), bf_hi(sv.z)));
-                  fma_pair(4 * q8 + 3, make_float2(bf_lo(sv.w), bf_hi(sv.w)));
-                }
               }
+              const uint32_t row = hb * 16384 + r * 128;
 #pragma unroll
               for (int q8 = 0; q8 < 8; ++q8) {
                 const uint32_t off = row + ((q8 ^ (r & 7)) << 4);
@@ -679,9 +684,9 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) kda_spec_mma_kernel(const Spec
                   *reinterpret_cast<uint4*>(lo + off) = yl;
                 }
               }
-              if (!last) {  // S' for the next chunk's epilogue
-                tc::st32(tl + CARRY_COL + 64 * hb, *reinterpret_cast<const float(*)[32]>(d));
-                tc::st32(tl + CARRY_COL + 64 * hb + 32, *reinterpret_cast<const float(*)[32]>(d + 32));
+              if (!last) {  // S' (float32) stays in the accumulator for the next chunk
+                tc::st32(acc + 64 * hb, *reinterpret_cast<const float(*)[32]>(d));
+                tc::st32(acc + 64 * hb + 32, *reinterpret_cast<const float(*)[32]>(d + 32));
               }
             }
             tc::fence_before_sync();
