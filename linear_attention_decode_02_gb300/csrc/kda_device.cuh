@@ -13,6 +13,17 @@ namespace kda {
 constexpr int kD = 128;           // head dimension K = V = 128
 constexpr float kL2Eps = 1e-6f;   // QK L2 normalisation epsilon
 
+// ---- programmatic dependent launch ------------------------------------------------
+
+// Returns once the previous kernel on the stream has completed and its memory
+// operations are visible (immediately when the grid was launched without
+// programmatic serialization).  Every kernel calls it before its first
+// global-memory access; only launch and on-chip set-up overlap the previous
+// kernel.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream begin its own launch and set-up.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---- bf16 <-> f32 ---------------------------------------------------------------
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }

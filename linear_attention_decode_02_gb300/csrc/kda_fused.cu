@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
   const int row0 = lane / G::LPR;
 
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)r * a.H + h) * kD;
+  pdl_wait();
+  pdl_launch_dependents();
   const int slot = __ldg(a.idx + r);
 
   // Operands that do not depend on the slot are requested before the slot
@@ -140,12 +142,9 @@ __global__ void __launch_bounds__(256, 2) kda_fused_kernel(const FusedArgs a) {
 
 cudaError_t launch_fused(const FusedArgs& a, int state_dtype, cudaStream_t s) {
   const int64_t blocks = (int64_t)a.rows * a.H;
-  if (state_dtype == KDA_DT_F32) {
-    kda_fused_kernel<float><<<dim3((unsigned)blocks), dim3(256), 0, s>>>(a);
-  } else {
-    kda_fused_kernel<__nv_bfloat16><<<dim3((unsigned)blocks), dim3(256), 0, s>>>(a);
-  }
-  return cudaGetLastError();
+  if (state_dtype == KDA_DT_F32)
+    return launch_pdl(kda_fused_kernel<float>, dim3((unsigned)blocks), dim3(256), 0, s, 1, a);
+  return launch_pdl(kda_fused_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(256), 0, s, 1, a);
 }
 
 }  // namespace kda

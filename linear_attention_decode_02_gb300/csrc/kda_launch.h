@@ -67,6 +67,36 @@ struct SpecArgs {
   int32_t t_cap;
 };
 
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic
+// stream serialization: the grid may begin (launch, CTA placement, on-chip
+// set-up) while the previous kernel on the stream drains; every kernel of this
+// library executes pdl_wait() before its first global-memory access, so
+// nothing the previous kernel writes is read early.  `cluster` > 1 adds a
+// thread-block cluster of that many CTAs along x.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int n = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    n = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Launchers: return the launch error (cudaSuccess on success).
 cudaError_t launch_t1(const T1Args& a, int state_dtype, int split, cudaStream_t s);
 cudaError_t launch_fused(const FusedArgs& a, int state_dtype, cudaStream_t s);

@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "kda_kernels.cuh"
+#include "kda_launch.h"
 #include "kda_packed_fused.h"
 
 namespace cg = cooperative_groups;
@@ -194,6 +195,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   auto sec_of = [](int lc) { return lc < kD ? 0 : (lc < 2 * kD ? 1 : 2); };
   auto cis_of = [slab0](int lc) { return lc < 2 * kD ? (lc & (kD - 1)) : slab0 + lc - 2 * kD; };
   __shared__ int4 s_pf;  // next unit: (start slot or 0, first token, end token, head)
+  pdl_wait();
+  pdl_launch_dependents();
 
   // Persistent: each cluster walks the units (sequence, head) with a stride
   // of the grid's cluster count; the padding slice is unit N*H .. (N+1)*H-1.
@@ -577,19 +580,7 @@ cudaError_t launch_packed_fused_variant(const PackedFusedArgs& a, int sms, cudaS
     }();
     clusters = std::min<int64_t>(units, (int64_t)per_sm * sms);
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(clusters * CL));
-  cfg.blockDim = dim3(NW * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = CL > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, kernel, a);
+  return launch_pdl(kernel, dim3((unsigned)(clusters * CL)), dim3(NW * 32), 0, s, CL, a);
 }
 
 template <typename StateT>

@@ -80,6 +80,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_spec_kernel
   const int row0 = lane / G::LPR;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)h * kD + col0;
   const int64_t out_rs = (int64_t)a.H * kD;
+  pdl_wait();
+  pdl_launch_dependents();
 
   if (n == a.N) {  // padding token rows
     const int lo = min(max(__ldg(a.cu), 0), a.R);
@@ -233,8 +235,7 @@ template <typename StateT, int CW, int NW, bool VERIFY>
 cudaError_t launch_spec_variant(const SpecArgs& a, cudaStream_t s) {
   constexpr int SPLIT = kD / (CW * NW);
   const int64_t blocks = (int64_t)(a.N + 1) * a.H * SPLIT;  // slice N zeroes padding rows
-  kda_spec_kernel<StateT, CW, NW, VERIFY><<<dim3((unsigned)blocks), dim3(NW * 32), 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kda_spec_kernel<StateT, CW, NW, VERIFY>, dim3((unsigned)blocks), dim3(NW * 32), 0, s, 1, a);
 }
 
 template <typename StateT, bool VERIFY>

@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(MMA_THREADS, 1) kda_spec_mma_kernel(const Spec
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int G = gridDim.x;
   const int n_my = (a.N * a.H - (int)blockIdx.x + G - 1) / G;  // units blockIdx.x + j * G
@@ -739,8 +741,7 @@ cudaError_t launch_spec_mma_variant(const SpecArgs& a, int sm_count, cudaStream_
   }
   const int64_t units = (int64_t)a.N * a.H;
   const int grid = (int)(units < sm_count ? (units > 0 ? units : 1) : sm_count);
-  kda_spec_mma_kernel<VERIFY><<<grid, MMA_THREADS, MMA_SMEM, s>>>(a, map);
-  return cudaGetLastError();
+  return launch_pdl(kda_spec_mma_kernel<VERIFY>, dim3(grid), dim3(MMA_THREADS), MMA_SMEM, s, 1, a, map);
 }
 
 }  // namespace

@@ -115,6 +115,8 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int P = gridDim.x;
   const int n_my = (units - (int)blockIdx.x + P - 1) / P;  // units blockIdx.x + j*P
@@ -310,6 +312,8 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
 
   const int P = gridDim.x;
   const int n_my = (units - (int)blockIdx.x + P - 1) / P;
@@ -534,6 +538,8 @@ __global__ void kda_selftest_wait_kernel() {
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait();
+  pdl_launch_dependents();
   const bool ok = mbar_wait(&bar, 0);
   if (!__all_sync(0xffffffffu, ok) && threadIdx.x == 0) record_error(4u);
 }
@@ -565,8 +571,8 @@ cudaError_t launch_t1_stream_typed(const T1Args& a, int sm_count, cudaStream_t s
   if (e != cudaSuccess) return e;
   const int units = a.B * a.H;
   const int grid = units < sm_count ? units : sm_count;
-  kda_t1_stream_kernel<StateT><<<grid, (T1Stream<StateT>::NW + 1 + T1_NP) * 32, smem, s>>>(a, map, units);
-  return cudaGetLastError();
+  return launch_pdl(kda_t1_stream_kernel<StateT>, dim3(grid), dim3((T1Stream<StateT>::NW + 1 + T1_NP) * 32), smem, s,
+                    1, a, map, units);
 }
 
 template <typename StateT>
@@ -579,9 +585,8 @@ cudaError_t launch_fused_stream_typed(const FusedArgs& a, int sm_count, cudaStre
   if (e != cudaSuccess) return e;
   const int units = a.rows * a.H;
   const int grid = units < sm_count ? units : sm_count;
-  kda_fused_stream_kernel<StateT><<<grid, (FusedStream<StateT>::NW + 1 + fused_np<StateT>()) * 32, smem, s>>>(
-      a, map, units);
-  return cudaGetLastError();
+  return launch_pdl(kda_fused_stream_kernel<StateT>, dim3(grid),
+                    dim3((FusedStream<StateT>::NW + 1 + fused_np<StateT>()) * 32), smem, s, 1, a, map, units);
 }
 
 }  // namespace

@@ -22,6 +22,8 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_t1_kernel(c
   const int col0 = (split * NW + warp) * CW + (lane % G::LPR) * G::VEC;
   const int row0 = lane / G::LPR;
   const int c4 = lane * 4;
+  pdl_wait();
+  pdl_launch_dependents();
 
   // Activation loads first: they do not depend on the slot.
   const float4 q = load4(a.q, (int64_t)b * a.q_rs + (int64_t)h * a.q_hs + c4, a.qkv_dtype);
@@ -72,8 +74,7 @@ template <typename StateT, int CW, int NW>
 cudaError_t launch_t1_variant(const T1Args& a, cudaStream_t s) {
   constexpr int SPLIT = kD / (CW * NW);
   const int64_t blocks = (int64_t)a.B * a.H * SPLIT;
-  kda_t1_kernel<StateT, CW, NW><<<dim3((unsigned)blocks), dim3(NW * 32), 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(kda_t1_kernel<StateT, CW, NW>, dim3((unsigned)blocks), dim3(NW * 32), 0, s, 1, a);
 }
 
 template <typename StateT>
