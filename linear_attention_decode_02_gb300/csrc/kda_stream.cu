@@ -78,23 +78,30 @@ constexpr uint32_t T1_ACT_SLOT = 512;  // one 128-vector, up to float32: q, k, v
 
 template <typename StateT>
 using T1Stream = StageCfg<StateT, 5 * T1_ACT_SLOT, sizeof(StateT) == 4 ? 3 : 5>;
+// bfloat16 state in halves: a work item is one 64-column TMA block of a unit,
+// which halves the last round's share of the persistent CTAs.
+template <typename StateT, int PARTS>
+using T1StreamP = StageCfg<StateT, 5 * T1_ACT_SLOT, PARTS == 1 ? (sizeof(StateT) == 4 ? 3 : 5) : 10, 0, PARTS>;
 // Prologue warps.  Units are dealt to them round-robin; NP must divide
 // NSTAGE so each stage is always served by the same prologue warp in round
 // order (a parity wait cannot tell a phase from the one two rounds later).
-constexpr int T1_NP = 1;
-
-template <typename StateT>
-__host__ __device__ constexpr size_t t1_stream_smem() {
-  return T1Stream<StateT>::TAIL_OFF + 1024;  // + base alignment slack
+template <int PARTS>
+__host__ __device__ constexpr int t1_np() {
+  return PARTS;  // every work item repeats its unit's coefficients: one prologue warp per part
 }
 
-template <typename StateT>
-__global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
-    kda_t1_stream_kernel(const T1Args a, const __grid_constant__ CUtensorMap state_map, const int units) {
-  using C = T1Stream<StateT>;
+template <typename StateT, int PARTS>
+__host__ __device__ constexpr size_t t1_stream_smem() {
+  return T1StreamP<StateT, PARTS>::TAIL_OFF + 1024;  // + base alignment slack
+}
+
+template <typename StateT, int PARTS>
+__global__ void __launch_bounds__((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PARTS>()) * 32, 1)
+    kda_t1_stream_kernel(const T1Args a, const __grid_constant__ CUtensorMap state_map, const int items) {
+  using C = T1StreamP<StateT, PARTS>;
   using G = Strip<StateT, C::CW>;
-  static_assert(t1_stream_smem<StateT>() <= 232448, "stages exceed the 227 KB shared memory of a CTA");
-  static_assert(C::NSTAGE % T1_NP == 0, "each stage must be served by one prologue warp");
+  static_assert(t1_stream_smem<StateT, PARTS>() <= 232448, "stages exceed the 227 KB shared memory of a CTA");
+  static_assert(C::NSTAGE % t1_np<PARTS>() == 0, "each stage must be served by one prologue warp");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -110,7 +117,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     for (int s = 0; s < C::NSTAGE; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&ready[s], 1);
-      mbar_init(&empty[s], C::NW);
+      mbar_init(&empty[s], C::GROUP_WARPS);
     }
     mbar_fence_init();
   }
@@ -119,7 +126,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
   pdl_launch_dependents();
 
   const int P = gridDim.x;
-  const int n_my = (units - (int)blockIdx.x + P - 1) / P;  // units blockIdx.x + j*P
+  const int n_my = (items - (int)blockIdx.x + P - 1) / P;  // items blockIdx.x + j*P; item i = unit i / PARTS
   const int qsz = a.qkv_dtype == KDA_DT_F32 ? 4 : 2;
   const int gsz = a.gate_dtype == KDA_DT_F32 ? 4 : 2;
 
@@ -128,8 +135,8 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     for (int j0 = 0; j0 < n_my; j0 += 32) {
       int slot = -1;
       float beta = 0.f, A = 0.f;
-      if (j0 + lane < n_my) {  // per-unit scalars, 32 units at a time
-        const int u = blockIdx.x + (j0 + lane) * P;
+      if (j0 + lane < n_my) {  // per-item scalars, 32 items at a time
+        const int u = (blockIdx.x + (j0 + lane) * P) / PARTS;
         const int h = u % a.H, b = u / a.H;
         slot = __ldg(a.idx + b);
         beta = sigmoidf_(load1(a.beta, (int64_t)b * a.b_rs + (int64_t)h * a.b_hs, a.beta_dtype));
@@ -149,16 +156,20 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
           return;
         }
         if (lane == 0) {
-          const int u = blockIdx.x + j * P;
+          const int item = blockIdx.x + j * P;
+          const int u = item / PARTS, part = item % PARTS;
           const int h = u % a.H, b = u / a.H;
           const bool live = slot_t > 0 && slot_t < a.num_slots;
           scal[s] = make_int4(live ? slot_t : -1, __float_as_int(beta_t), __float_as_int(A_t), 0);
           if (live) {
             unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
             const uint32_t qb = kD * qsz, gb = kD * gsz;
-            mbar_arrive_expect_tx(&full[s], C::STATE_BYTES + 3 * qb + gb + kD * 4);
-            tma_load_state<StateT>(st, &state_map, h, slot_t, &full[s]);
-            unsigned char* act = st + C::STATE_BYTES;
+            mbar_arrive_expect_tx(&full[s], C::PART_BYTES + 3 * qb + gb + kD * 4);
+#pragma unroll
+            for (int blk = 0; blk < C::PART_BLKS; ++blk)
+              tma_load_3d(st + blk * C::BLK_BYTES, &state_map, (part * C::PART_BLKS + blk) * C::BLK_COLS, h * kD,
+                          slot_t, &full[s]);
+            unsigned char* act = st + C::PART_BYTES;
             const char* q = static_cast<const char*>(a.q) + ((int64_t)b * a.q_rs + (int64_t)h * a.q_hs) * qsz;
             const char* k = static_cast<const char*>(a.k) + ((int64_t)b * a.k_rs + (int64_t)h * a.k_hs) * qsz;
             const char* v = static_cast<const char*>(a.v) + ((int64_t)b * a.v_rs + (int64_t)h * a.v_hs) * qsz;
@@ -180,7 +191,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
 
   if (warp > C::NW) {
     // ---------------- prologue warps (units round-robin): per-key-channel coefficients, once ----------------
-    for (int j = warp - C::NW - 1; j < n_my; j += T1_NP) {
+    for (int j = warp - C::NW - 1; j < n_my; j += t1_np<PARTS>()) {
       const int s = j % C::NSTAGE;
       const bool ok = mbar_wait(&full[s], (j / C::NSTAGE) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -189,7 +200,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       }
       const int4 sc = scal[s];
       if (sc.x >= 0) {
-        const unsigned char* act = smem + (size_t)s * C::STAGE_BYTES + C::STATE_BYTES;
+        const unsigned char* act = smem + (size_t)s * C::STAGE_BYTES + C::PART_BYTES;
         const float A = __int_as_float(sc.z);
         const float4 q = lds4(act, 4 * lane, a.qkv_dtype);
         const float4 k = lds4(act + T1_ACT_SLOT, 4 * lane, a.qkv_dtype);
@@ -209,10 +220,10 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     return;
   }
 
-  // ---------------- consumers ----------------
-  const int col0 = warp * C::CW + (lane % G::LPR) * G::VEC;
-  const int row0 = stream_row0<StateT>(lane);
-  for (int j = 0; j < n_my; ++j) {
+  // ---------------- consumers: group warp / GROUP_WARPS takes items j = group, group + PARTS, ... ----------------
+  const int col0 = (warp % C::GROUP_WARPS) * C::CW + (lane % G::LPR) * G::VEC;  // column within the staged part
+  const int row0 = stream_row0<G::LPR>(lane);
+  for (int j = warp / C::GROUP_WARPS; j < n_my; j += PARTS) {
     const int s = j % C::NSTAGE;
     const uint32_t par = (j / C::NSTAGE) & 1;
     const bool ok = mbar_wait(&full[s], par) && mbar_wait(&ready[s], par);
@@ -220,12 +231,14 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       if (lane == 0) record_error(1u);
       return;
     }
-    const int u = blockIdx.x + j * P;
+    const int item = blockIdx.x + j * P;
+    const int u = item / PARTS;
+    const int gcol = (item % PARTS) * C::PART_COLS + col0;  // column within the unit
     const int h = u % a.H, b = u / a.H;
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)b * a.H + h) * kD;
     const int4 sc = scal[s];
     if (sc.x < 0) {  // null row: zero output, no cache access
-      if (row0 == 0) store_out_zero<G::VEC>(out + col0);
+      if (row0 == 0) store_out_zero<G::VEC>(out + gcol);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       continue;
@@ -236,7 +249,7 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
     float vv[G::VEC];
 #pragma unroll
     for (int jj = 0; jj < G::VEC; jj += 4) {
-      const float4 t = lds4(st + C::STATE_BYTES + 2 * T1_ACT_SLOT, col0 + jj, a.qkv_dtype);
+      const float4 t = lds4(st + C::PART_BYTES + 2 * T1_ACT_SLOT, gcol + jj, a.qkv_dtype);
       vv[jj] = t.x; vv[jj + 1] = t.y; vv[jj + 2] = t.z; vv[jj + 3] = t.w;
     }
     // k-reductions; the decay and key coefficients of each row stay in registers
@@ -256,8 +269,8 @@ __global__ void __launch_bounds__((T1Stream<StateT>::NW + 1 + T1_NP) * 32, 1)
       o[jj] = a.scale * (acc_b[jj] + qk * u_[jj]);
     }
     StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
-    update_store_regs<StateT, G>(sp, row0, col0, S, dk, u_);
-    if (row0 == 0) store_out<G::VEC>(out + col0, o);
+    update_store_regs<StateT, G>(sp, row0, gcol, S, dk, u_);
+    if (row0 == 0) store_out<G::VEC>(out + gcol, o);
   }
 }
 
@@ -455,7 +468,7 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
 
   // ---------------- consumers ----------------
   const int col0 = warp * C::CW + (lane % G::LPR) * G::VEC;
-  const int row0 = stream_row0<StateT>(lane);
+  const int row0 = stream_row0<G::LPR>(lane);
   float nw[G::VEC];
 #pragma unroll
   for (int jj = 0; jj < G::VEC; ++jj) nw[jj] = __ldg(a.norm_w + col0 + jj);
@@ -561,18 +574,18 @@ cudaError_t ensure_smem(Kernel k, size_t bytes, bool* set_flags) {
   return cudaSuccess;
 }
 
-template <typename StateT>
+template <typename StateT, int PARTS>
 cudaError_t launch_t1_stream_typed(const T1Args& a, int sm_count, cudaStream_t s) {
   CUtensorMap map;
   if (!encode_state_map<StateT>(&map, a.state, a.H, a.num_slots, a.slot_stride)) return cudaErrorNotSupported;
   static bool set[64] = {};
-  constexpr size_t smem = t1_stream_smem<StateT>();
-  cudaError_t e = ensure_smem(kda_t1_stream_kernel<StateT>, smem, set);
+  constexpr size_t smem = t1_stream_smem<StateT, PARTS>();
+  cudaError_t e = ensure_smem(kda_t1_stream_kernel<StateT, PARTS>, smem, set);
   if (e != cudaSuccess) return e;
-  const int units = a.B * a.H;
-  const int grid = units < sm_count ? units : sm_count;
-  return launch_pdl(kda_t1_stream_kernel<StateT>, dim3(grid), dim3((T1Stream<StateT>::NW + 1 + T1_NP) * 32), smem, s,
-                    1, a, map, units);
+  const int items = a.B * a.H * PARTS;
+  const int grid = items < sm_count ? items : sm_count;
+  return launch_pdl(kda_t1_stream_kernel<StateT, PARTS>, dim3(grid),
+                    dim3((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PARTS>()) * 32), smem, s, 1, a, map, items);
 }
 
 template <typename StateT>
@@ -592,8 +605,8 @@ cudaError_t launch_fused_stream_typed(const FusedArgs& a, int sm_count, cudaStre
 }  // namespace
 
 cudaError_t launch_t1_stream(const T1Args& a, int state_dtype, int sm_count, cudaStream_t s) {
-  if (state_dtype == KDA_DT_F32) return launch_t1_stream_typed<float>(a, sm_count, s);
-  return launch_t1_stream_typed<__nv_bfloat16>(a, sm_count, s);
+  if (state_dtype == KDA_DT_F32) return launch_t1_stream_typed<float, 1>(a, sm_count, s);
+  return launch_t1_stream_typed<__nv_bfloat16, 2>(a, sm_count, s);
 }
 
 cudaError_t launch_fused_stream(const FusedArgs& a, int state_dtype, int sm_count, cudaStream_t s) {

@@ -21,35 +21,51 @@ struct SwzCfg {
   static constexpr uint32_t STATE_BYTES = NBLK * BLK_BYTES;
 };
 
-// Ring of NSTAGE stages: [state block | ACT_BYTES of unit vectors] each
+// Ring of NSTAGE stages: [state part | ACT_BYTES of unit vectors] each
 // (1024-byte aligned), then per stage a coefficient array (128 float4),
 // DERIVED_BYTES of prologue results, scalars (int4) and three mbarriers.
-template <typename StateT, uint32_t ACT_BYTES, int NSTAGE_, uint32_t DERIVED_BYTES = 0>
+// PARTS > 1 splits a unit's value columns into that many work items of
+// 128 / PARTS columns (whole TMA column blocks), each staged on its own; the
+// consumer warps then form PARTS groups of NW / PARTS warps that take the
+// items in turn, each warp keeping a 16-column strip (whole 32-byte row
+// segments for bf16, so every state store fills a sector).
+template <typename StateT, uint32_t ACT_BYTES, int NSTAGE_, uint32_t DERIVED_BYTES = 0, int PARTS_ = 1>
 struct StageCfg : SwzCfg<StateT> {
   static constexpr int NSTAGE = NSTAGE_;
-  static constexpr int NW = 8;   // consumer warps
-  static constexpr int CW = 16;  // columns per consumer warp
-  static constexpr uint32_t STAGE_BYTES = ((SwzCfg<StateT>::STATE_BYTES + ACT_BYTES + 1023) / 1024) * 1024;
+  static constexpr int PARTS = PARTS_;
+  static constexpr int NW = 8;            // consumer warps
+  static constexpr int CW = 16;           // columns per consumer warp
+  static constexpr int GROUP_WARPS = NW / PARTS;  // consumer warps per item
+  static constexpr int PART_COLS = kD / PARTS;
+  static constexpr int PART_BLKS = SwzCfg<StateT>::NBLK / PARTS;  // TMA column blocks of a part
+  static constexpr uint32_t PART_BYTES = SwzCfg<StateT>::STATE_BYTES / PARTS;
+  static_assert(PART_BLKS >= 1 && PART_BLKS * PARTS == SwzCfg<StateT>::NBLK, "parts must be whole column blocks");
+  static constexpr uint32_t STAGE_BYTES = ((PART_BYTES + ACT_BYTES + 1023) / 1024) * 1024;
   static constexpr size_t COEF_OFF = (size_t)NSTAGE * STAGE_BYTES;
   static constexpr size_t DERIVED_OFF = COEF_OFF + (size_t)NSTAGE * kD * sizeof(float4);
   static constexpr size_t SCAL_OFF = DERIVED_OFF + (size_t)NSTAGE * DERIVED_BYTES;
   static constexpr size_t BAR_OFF = SCAL_OFF + (size_t)NSTAGE * sizeof(int4);
   static constexpr size_t TAIL_OFF = BAR_OFF + 3 * NSTAGE * sizeof(uint64_t);  // kernel-specific extras
-  static_assert(CW * NW == kD, "consumers cover the 128 value columns");
+  static_assert(CW * GROUP_WARPS * PARTS == kD, "a consumer group covers a part's value columns");
 };
 
-// Lane -> first key row of its fragments, chosen so that the rows read by
-// one quarter-warp differ in bit 2 (f32: 2 rows) or bits 1-2 (bf16: 4 rows):
+// Lane -> first key row of its fragments for LPR lanes per row segment,
+// chosen so that the rows read by one quarter-warp differ in bit 2 (4 lanes
+// per row: 2 rows), bits 1-2 (2 lanes: 4 rows) or bits 0-2 (1 lane: 8 rows):
 // under the 128-byte swizzle those rows' chunks land in distinct banks.
-template <typename StateT>
+template <int LPR>
 __device__ __forceinline__ int stream_row0(int lane);
 template <>
-__device__ __forceinline__ int stream_row0<float>(int lane) {  // 4 lanes per row, 8 rows per instruction
+__device__ __forceinline__ int stream_row0<4>(int lane) {  // 8 rows per instruction
   return (lane >> 3) + ((lane >> 2) & 1) * 4;
 }
 template <>
-__device__ __forceinline__ int stream_row0<__nv_bfloat16>(int lane) {  // 2 lanes per row, 16 rows
+__device__ __forceinline__ int stream_row0<2>(int lane) {  // 16 rows per instruction
   return ((lane >> 1) & 3) * 2 + ((lane >> 3) & 1) + ((lane >> 4) & 1) * 8;
+}
+template <>
+__device__ __forceinline__ int stream_row0<1>(int lane) {  // 32 rows per instruction
+  return lane;
 }
 
 // Byte offset of the 16-byte chunk holding (row, col) in a swizzled state block.
