@@ -119,8 +119,11 @@ def kernel_source(op, units, state_dtype):
     """Translation unit of the kernel the library's dispatch picks for this call shape."""
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     code = 0 if state_dtype == torch.float32 else 1
-    if binding.kda_plan_schedule(op, units, code, 1, sms) == binding.SCHED_STREAM:
+    sched = binding.kda_plan_schedule(op, units, code, 1, sms)
+    if sched == binding.SCHED_STREAM:
         return "kda_stream.cu"
+    if sched == binding.SCHED_MMA:
+        return "kda_spec_mma.cu"
     return SPLIT_SOURCE[op]
 
 
@@ -291,7 +294,8 @@ def make_workload(args, seed):
     if args.workload == "packed_fused":
         return PackedFused(N=args.batch or 128, T=args.t_max or 5, H=args.heads or 12,
                            state_dtype=torch.bfloat16 if args.bf16_state else torch.float32, seed=seed)
-    return Spec(N=args.batch or 128, t_max=args.t_max or 6, H=args.heads or 16, slots=args.slots, seed=seed)
+    return Spec(N=args.batch or 128, t_max=args.t_max or 6, H=args.heads or 16, slots=args.slots, seed=seed,
+                state_dtype=torch.bfloat16 if args.bf16_state else torch.float32, fixed=args.fixed)
 
 
 # ---- environment -------------------------------------------------------------------
@@ -761,7 +765,10 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=("recurrent", "packed", "fused", "spec", "packed_fused"),
                     default="recurrent")
-    ap.add_argument("--bf16-state", action="store_true", help="packed_fused: bfloat16 state pool")
+    ap.add_argument("--bf16-state", action="store_true", help="packed_fused, spec: bfloat16 state pool")
+    ap.add_argument("--fixed", action="store_true", help="spec: every row exactly --t-max tokens")
+    ap.add_argument("--schedule", choices=("auto", "split", "stream", "mma"), default="auto",
+                    help="force a kernel schedule (mma: the tensor-core speculative form, bf16 state)")
     ap.add_argument("--batch", type=int, default=0, help="rows (B / rows / N); 0 = the workload's default")
     ap.add_argument("--heads", type=int, default=0)
     ap.add_argument("--slots", type=int, default=0)
@@ -803,6 +810,8 @@ def main():
     peak = float(peaks["hbm_gbs"]) if peaks and peaks.get("hbm_gbs") else FALLBACK_HBM_GBS
     peak_src = "measured" if peaks and peaks.get("hbm_gbs") else "fallback"
 
+    binding.kda_set_schedule_override({"auto": binding.SCHED_AUTO, "split": binding.SCHED_SPLIT,
+                                       "stream": binding.SCHED_STREAM, "mma": binding.SCHED_MMA}[args.schedule])
     wl = make_workload(args, seed=rank)
     clocks = clock_sampler(torch.cuda.current_device())
     clocks.start()
@@ -830,6 +839,10 @@ def main():
         e2e_obj = {"value": round(job_gbs(wl.nbytes, world, e_max), 1), "unit": "GB/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e_max, 5)}
     name, cfg, nbytes, source = wl.name, dict(wl.config), wl.nbytes, wl.source
+    if args.schedule != "auto":
+        cfg["schedule"] = args.schedule
+        name += "_" + args.schedule
+    binding.kda_set_schedule_override(binding.SCHED_AUTO)
     del wl
     torch.cuda.empty_cache()
 
