@@ -266,7 +266,9 @@ typedef enum kda_op {
  * unit.  Returns the split (1, 2, 4, 8 or 16), or 0 on invalid arguments.
  * Honors kda_set_split_override.  For KDA_OP_PACKED_FUSED (units =
  * sequences * heads) the split is the size of the thread-block cluster that
- * shares a unit (1, 2, 4 or 8; a forced 16 runs as 8).
+ * shares a unit (1, 2, 4 or 8; a forced 16 runs as 8); for KDA_OP_FUSED it
+ * is the cluster size of the split schedule: 1 unless forced (2 or 4; a
+ * forced 8 or 16 runs as 4).
  */
 int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t_max,
                        int32_t sm_count);
@@ -274,8 +276,7 @@ int32_t kda_plan_split(int32_t op, int64_t units, int32_t state_dtype, int32_t t
 /*
  * Force the split of every later call in this process (0 restores the
  * measured policy).  For sweeps and tests.  Returns KDA_ERR_INVALID_ARG for
- * a split this build has no kernel for (the fused entry point always uses
- * split 1 and ignores the override).  A forced split selects the split
+ * a split this build has no kernel for.  A forced split selects the split
  * schedule for the T=1 entry points unless a schedule is forced too.
  */
 kda_status kda_set_split_override(int32_t split);
@@ -283,8 +284,9 @@ kda_status kda_set_split_override(int32_t split);
 /*
  * Kernel schedules of the T=1 entry points (kda_recurrent_decode,
  * kda_packed_decode, kda_fused_decode).  SPLIT: one CTA per (row, head,
- * value split; the fused entry point always uses one split), the state
- * block streamed through registers; best for latency-bound batches.
+ * value split; the fused entry point's splits form a thread-block cluster
+ * that shares the RMSNorm), the state block streamed through registers;
+ * best for latency-bound batches.
  * STREAM: one persistent CTA per SM, a loader warp moving whole state
  * blocks (TMA, swizzled) and the unit's activation vectors into
  * shared-memory stages with bulk asynchronous copies while consumer warps

@@ -308,7 +308,12 @@ int plan_cluster(int64_t units, int state_dtype, int sms) {
 int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {
   (void)t_max;
   const int forced = g_split_override.load();
-  if (op == KDA_OP_FUSED) return 1;
+  // Fused split schedule: cluster of CTAs per (row, head).  Measured on
+  // GB300, one CTA is never slower than 2 or 4 (H=8 N=1: 5.4 / 5.7 / 5.8 us;
+  // H=32 N=4: 6.0 / 7.2 / 8.3 us): a small batch waits on the chain slot ->
+  // state and conv cache -> update -> store, which a split does not shorten,
+  // and the cluster barriers add to it.  Clusters only when forced.
+  if (op == KDA_OP_FUSED) return forced == 0 ? 1 : (forced > 4 ? 4 : forced);
   if (forced != 0) return op == KDA_OP_PACKED_FUSED ? (forced > 8 ? 8 : forced) : forced;
   // Measured on GB300 for the split kernel: speculative rows (T tokens of
   // work per state block) 2 value slabs per unit at every size; T=1 with
@@ -592,7 +597,8 @@ kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, 
   a.lower_bound = lower_bound; a.norm_eps = norm_eps;
   a.scale = 0.08838834764831845f;  // 1/sqrt(128)
   if (sched == KDA_SCHED_STREAM) return check_launch(kda::launch_fused_stream(a, S.dtype, dev.sms, st));
-  return check_launch(kda::launch_fused(a, S.dtype, st));
+  const int cluster = plan_split(KDA_OP_FUSED, rows * H, S.dtype, 1, dev.sms);
+  return check_launch(kda::launch_fused(a, S.dtype, cluster, st));
 }
 
 kda_status kda_packed_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, const kda_tensor* conv_state,

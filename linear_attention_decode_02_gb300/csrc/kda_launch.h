@@ -99,7 +99,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Launchers: return the launch error (cudaSuccess on success).
 cudaError_t launch_t1(const T1Args& a, int state_dtype, int split, cudaStream_t s);
-cudaError_t launch_fused(const FusedArgs& a, int state_dtype, cudaStream_t s);
+// `cluster` CTAs (1, 2 or 4) share each (row, head), one value slab each.
+cudaError_t launch_fused(const FusedArgs& a, int state_dtype, int cluster, cudaStream_t s);
 cudaError_t launch_spec(const SpecArgs& a, int state_dtype, int split, bool verify, cudaStream_t s);
 
 // Persistent streaming T=1 kernel (bulk copies into shared-memory stages);

@@ -62,7 +62,8 @@ def test_plan_split_policy(lib):
     assert binding.kda_plan_split(0, 760, 0, 1, 152) == 4
     assert binding.kda_plan_split(3, 2048, 0, 6, 152) == 2
     assert binding.kda_plan_split(3, 16, 0, 6, 152) == 2
-    assert binding.kda_plan_split(2, 8, 0, 1, 152) == 1  # fused is always split 1
+    for units in (1, 8, 38, 76, 77, 16384):  # fused: one CTA per unit unless a cluster is forced
+        assert binding.kda_plan_split(2, units, 0, 1, 152) == 1
     assert binding.kda_plan_split(0, 1, 5, 1, 152) == 0  # bad dtype
     assert binding.kda_plan_split(9, 1, 0, 1, 152) == 0  # bad op
     for units in (1, 3, 12, 100, 1000, 100000):
@@ -74,7 +75,9 @@ def test_split_override(lib):
     assert lib.kda_set_split_override(3) == INVALID
     assert lib.kda_set_split_override(4) == OK
     assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
-    assert binding.kda_plan_split(2, 16384, 0, 1, 152) == 1
+    assert binding.kda_plan_split(2, 16384, 0, 1, 152) == 4
+    assert lib.kda_set_split_override(16) == OK
+    assert binding.kda_plan_split(2, 16384, 0, 1, 152) == 4  # a forced 8 or 16 runs as 4
     assert lib.kda_set_split_override(0) == OK
     assert binding.kda_plan_split(0, 16384, 0, 1, 152) == 4
 

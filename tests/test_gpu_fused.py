@@ -181,3 +181,49 @@ def test_fused_stream_rejects_unaligned_rows(stream_schedule):
     with pytest.raises(binding.KdaError) as e:
         _run(d)
     assert e.value.status == 2
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4])
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("lower_bound", [-5.0, None])
+def test_fused_every_cluster_size(cluster, state_dtype, lower_bound):
+    """The split schedule with 1, 2 or 4 CTAs per (row, head): each CTA owns a
+    slab of the value columns, the RMSNorm sums meet through distributed
+    shared memory, and each conv-cache channel is shifted by exactly one CTA."""
+    binding.kda_set_split_override(cluster)
+    try:
+        case = synth.fused_case(12, 7, seed=70 + cluster, state_dtype=state_dtype, null_frac=0.3)
+        d = _device_case(case)
+        before, cbefore = d["state"].clone(), d["conv_state"].clone()
+        out = torch.full((1, 7, 12, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+        _run(d, lower_bound=lower_bound, out=out)
+        torch.cuda.synchronize()
+    finally:
+        binding.kda_set_split_override(0)
+    _check(case, d, before, cbefore, out, lower_bound=lower_bound)
+
+
+@pytest.mark.parametrize("cluster", [2, 4])
+def test_fused_cluster_repeated_calls_are_identical(cluster):
+    """Every CTA of a cluster reads the conv history of all q and k channels
+    while the owning CTA shifts it: fifty calls from the same caches must give
+    the same outputs and caches bit for bit."""
+    binding.kda_set_split_override(cluster)
+    try:
+        case = synth.fused_case(8, 3, seed=80 + cluster, null_frac=0.0)
+        d = _device_case(case)
+        st0, cs0 = d["state"].clone(), d["conv_state"].clone()
+        first = None
+        for _ in range(50):
+            d["state"].copy_(st0)
+            d["conv_state"].copy_(cs0)
+            out = _run(d)
+            torch.cuda.synchronize()
+            got = (out.clone(), d["state"].clone(), d["conv_state"].clone())
+            if first is None:
+                first = got
+                _check(case, d, st0, cs0, out)
+            else:
+                assert all(torch.equal(x, y) for x, y in zip(got, first))
+    finally:
+        binding.kda_set_split_override(0)
