@@ -554,21 +554,11 @@ def time_graph(wl, n_calls, reps, flush):
     return statistics.median(times)
 
 
-def e2e(wl, steps, warmup, barrier):
-    """The same call end to end: every step copies its activations and slot
-    indices from pinned host memory to the device and its output back.
-
-    The steps are pipelined the way a serving loop would run them: a step's
-    inputs sit in one pinned staging buffer and cross in one host-to-device
-    copy (the entry point then takes views into the device copy); inputs and
-    outputs are double-buffered on the device, host-to-device copies run on
-    one side stream and device-to-host copies on another, and events keep
-    step i's copies ordered with its kernel; the state pool is updated in
-    place on the compute stream, so kernels stay in order.
-    """
+def _staging(wl):
+    """Pinned host staging of a step's inputs: each input and the slot indices
+    at 256-byte aligned offsets of one buffer (one buffer per slot set), and a
+    function giving the typed views of such a buffer."""
     keys = list(wl.e2e_keys)
-    nb = 2
-    # staging layout: each input and the slot indices at 256-byte aligned offsets
     fields, off = [], 0
     for k in keys + ["__idx__"]:
         t = wl.sets[0] if k == "__idx__" else wl.d[k]
@@ -581,13 +571,30 @@ def e2e(wl, steps, warmup, barrier):
         return {k: buf[o:o + n].view(dt).view(shape) for k, o, n, dt, shape in fields}
 
     host = []
-    for idx in wl.sets:  # one staging buffer per slot set: the step's inputs as they arrive
+    for idx in wl.sets:
         hb = torch.empty(total, dtype=torch.uint8).pin_memory()
         hv = views(hb)
         for k in keys:
             hv[k].copy_(wl.d[k].cpu())
         hv["__idx__"].copy_(idx.cpu())
         host.append(hb)
+    return keys, fields, total, views, host
+
+
+def e2e(wl, steps, warmup, barrier):
+    """The same call end to end: every step copies its activations and slot
+    indices from pinned host memory to the device and its output back.
+
+    The steps are pipelined the way a serving loop would run them: a step's
+    inputs sit in one pinned staging buffer and cross in one host-to-device
+    copy (the entry point then takes views into the device copy); inputs and
+    outputs are double-buffered on the device, host-to-device copies run on
+    one side stream and device-to-host copies on another, and events keep
+    step i's copies ordered with its kernel; the state pool is updated in
+    place on the compute stream, so kernels stay in order.
+    """
+    keys, fields, total, views, host = _staging(wl)
+    nb = 2
     dev = [torch.empty(total, dtype=torch.uint8, device="cuda") for _ in range(nb)]
     dv = [views(d) for d in dev]
     outs = [torch.empty_like(wl.out) for _ in range(nb)]
@@ -668,6 +675,56 @@ def path_measurements(flush, peak):
     for H, N in ((12, 1), (12, 8), (12, 32), (12, 128), (24, 8), (24, 128)):
         for dt in (torch.float32, torch.bfloat16):
             run(PackedFused(N=N, T=5, H=H, state_dtype=dt, n_sets=2, seed=H + N), 2)
+    torch.cuda.empty_cache()
+    return res
+
+
+def e2e_serial(wl, steps, warmup):
+    """End to end on one stream, one step after another, driven from Python
+    (no CUDA graph): the step's inputs in one copy from pinned host memory,
+    the entry point (descriptor marshalling, validation, launch), the output
+    copied back to pinned memory.  Returns ms per step and the bytes each way."""
+    keys, fields, total, views, host = _staging(wl)
+    dev = torch.empty(total, dtype=torch.uint8, device="cuda")
+    dv = views(dev)
+    base = dict(wl.d)
+    wl.d = {**base, **{k: dv[k] for k in keys}}
+    out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype).pin_memory()
+
+    def step(i):
+        dev.copy_(host[i % len(host)], non_blocking=True)
+        wl.call(dv["__idx__"])
+        out_h.copy_(wl.out, non_blocking=True)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(warmup, warmup + steps):
+        step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    wl.d = base
+    return e0.elapsed_time(e1) / steps, sum(n for _, _, n, _, _ in fields), out_h.numel() * out_h.element_size()
+
+
+def small_e2e():
+    """End to end at small batches (`e2e_serial`).  At these sizes the host
+    work, not the kernel, sets the pace; `paths` times the same kernels from
+    a CUDA graph."""
+    res = {}
+    makers = (lambda: Recurrent(B=1, H=32, slots=64, n_sets=2, seed=1),
+              lambda: Recurrent(B=8, H=32, slots=64, n_sets=2, seed=8),
+              lambda: Packed(B=1, slots=64, n_sets=2, seed=1),
+              lambda: Fused(H=8, rows=1, n_sets=2, seed=9),
+              lambda: Spec(N=1, t_max=6, H=16, n_sets=2, seed=7),
+              lambda: PackedFused(N=1, T=5, H=12, state_dtype=torch.bfloat16, n_sets=2, seed=13))
+    for make in makers:
+        wl = make()
+        ms, h2d, d2h = e2e_serial(wl, 300, 30)
+        res[wl.name] = {"us": round(ms * 1e3, 2), "h2d_bytes": h2d, "d2h_bytes": d2h}
+        del wl
     torch.cuda.empty_cache()
     return res
 
@@ -846,11 +903,12 @@ def main():
     del wl
     torch.cuda.empty_cache()
 
-    paths = None
+    paths = small = None
     if not args.no_paths and rank == 0:
         flush = L2Flush()
         paths = path_measurements(flush, peak)
         del flush
+        small = small_e2e()
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
@@ -872,7 +930,7 @@ def main():
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": ncu_traffic(name), "kernel": name,
                          "peak_source": f"{peak_src} copy bandwidth (burst)"},
-            "e2e": e2e_obj, "clocks": clock_rec, "cpu_baseline": cpu, "paths": paths,
+            "e2e": e2e_obj, "clocks": clock_rec, "cpu_baseline": cpu, "paths": paths, "e2e_small": small,
             "kernel_source": source, "kernel_source_hash": kernel_source_hash(source),
         }
         print(json.dumps(line))

@@ -9,6 +9,7 @@ first call raises.
 
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -90,6 +91,8 @@ def _declare(lib):
 def library(path=None):
     """Load (once) and return the ctypes handle of libkda.so."""
     global _lib
+    if _lib is not None and path is None:
+        return _lib
     with _lock:
         if _lib is None:
             p = path or _LIB_PATH
@@ -125,17 +128,35 @@ _DESC_CACHE_MAX = 1024
 
 def _ref(t):
     key = (t.data_ptr(), t.dtype, t.shape, t.stride())
-    d = _DESC_CACHE.get(key)
-    if d is None:
-        d = desc(t)
+    r = _DESC_CACHE.get(key)
+    if r is None:
+        r = ctypes.byref(desc(t))  # holds the descriptor alive
         if len(_DESC_CACHE) >= _DESC_CACHE_MAX:
             _DESC_CACHE.clear()
-        _DESC_CACHE[key] = d
-    return ctypes.byref(d)
+        _DESC_CACHE[key] = r
+    return r
+
+
+# The current stream's raw handle without building a torch.cuda.Stream
+# object (2.2 -> 0.1 us a call on the Grace host); the public query where
+# the raw one is absent.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
 def _stream(t):
+    if _raw_stream is not None and t.device.type == "cuda":
+        return ctypes.c_void_p(_raw_stream(t.device.index))
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+_SAME_DEVICE = contextlib.nullcontext()
+
+
+def _on(dev):
+    """Device guard for the call, entered only when `dev` is not already current."""
+    if dev.type == "cuda" and dev.index == torch.cuda.current_device():
+        return _SAME_DEVICE
+    return torch.cuda.device(dev)
 
 
 def _check(lib, status):
@@ -149,7 +170,7 @@ def kda_recurrent_decode(q, k, v, raw_gate, raw_beta, A_log, dt_bias, state_indi
     lib = library()
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         st = lib.kda_recurrent_decode(_ref(q), _ref(k), _ref(v), _ref(raw_gate), _ref(raw_beta),
                                       _ref(A_log), _ref(dt_bias), _ref(state_indices), _ref(state),
                                       _ref(out), int(lower_bound is not None),
@@ -164,7 +185,7 @@ def kda_packed_decode(mixed_qkv, raw_gate, raw_beta, A_log, dt_bias, state_indic
     lib = library()
     if out is None:
         out = torch.empty((mixed_qkv.shape[0], 1, 12, 128), dtype=torch.bfloat16, device=mixed_qkv.device)
-    with torch.cuda.device(mixed_qkv.device):
+    with _on(mixed_qkv.device):
         st = lib.kda_packed_decode(_ref(mixed_qkv), _ref(raw_gate), _ref(raw_beta), _ref(A_log),
                                    _ref(dt_bias), _ref(state_indices), _ref(state), _ref(out),
                                    _stream(mixed_qkv))
@@ -179,7 +200,7 @@ def kda_fused_decode(x, conv_weight, conv_state, raw_gate, raw_beta, A_log, dt_b
     if out is None:
         H = state.shape[1]
         out = torch.empty((1, x.shape[0], H, 128), dtype=torch.bfloat16, device=x.device)
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.kda_fused_decode(_ref(x), _ref(conv_weight), _ref(conv_state), _ref(raw_gate),
                                   _ref(raw_beta), _ref(A_log), _ref(dt_bias), _ref(state_indices),
                                   _ref(state), _ref(output_gate), _ref(norm_weight),
@@ -197,7 +218,7 @@ def kda_packed_fused_decode(x, conv_weight, conv_state, raw_gate, raw_beta, A_lo
     lib = library()
     if out is None:
         out = torch.empty((x.shape[0], state.shape[1], 128), dtype=torch.bfloat16, device=x.device)
-    with torch.cuda.device(x.device):
+    with _on(x.device):
         st = lib.kda_packed_fused_decode(_ref(x), _ref(conv_weight), _ref(conv_state), _ref(raw_gate),
                                          _ref(raw_beta), _ref(A_log), _ref(dt_bias), _ref(state_indices),
                                          _ref(query_start_loc), _ref(num_accepted_tokens), _ref(state),
@@ -214,7 +235,7 @@ def kda_spec_decode(q, k, v, g, beta, cu_seqlens, state_indices, state, t_max, o
     lib = library()
     if out is None:
         out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         st = lib.kda_spec_decode(_ref(q), _ref(k), _ref(v), _ref(g), _ref(beta), int(bool(beta_is_logit)),
                                  _ref(cu_seqlens), int(t_max), _ref(state_indices), _ref(state),
                                  _ref(out), float(scale), _stream(q))
@@ -230,7 +251,7 @@ def kda_spec_verify_decode(q, k, v, g, beta, cu_seqlens, state_indices, state, t
         out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
     cc = _ref(correction_cache) if correction_cache is not None else None
     kg = _ref(kg_cache) if kg_cache is not None else None
-    with torch.cuda.device(q.device):
+    with _on(q.device):
         st = lib.kda_spec_verify_decode(_ref(q), _ref(k), _ref(v), _ref(g), _ref(beta), int(bool(beta_is_logit)),
                                         _ref(cu_seqlens), int(t_max), _ref(state_indices), _ref(state), _ref(out),
                                         cc, kg, float(scale), _stream(q))
