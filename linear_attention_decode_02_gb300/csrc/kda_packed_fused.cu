@@ -164,10 +164,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   static_assert(W % 8 == 0, "slabs are staged in 16-byte pieces");
   // The staged conv input (read in phase A) and the raw outputs (written in
   // phase C) share one buffer.
+  // The conv's raw inputs of a channel in one column, oldest first: rows 0-2
+  // the history, rows 3 .. 3 + nt - 1 the staged chunk rows (q | k | v slab).
+  // The raw outputs (phase C) reuse the staged rows, never the history.
   constexpr int XO_BYTES = TC * NCH * 2 > TC * W * 4 ? TC * NCH * 2 : TC * W * 4;
-  __shared__ __align__(16) unsigned char s_xo[XO_BYTES];
-  auto s_x = reinterpret_cast<__nv_bfloat16 (*)[NCH]>(s_xo);  // staged conv input: q | k | v slab
-  auto s_o = reinterpret_cast<float (*)[W]>(s_xo);            // raw outputs (slab)
+  constexpr int HIST_BYTES = 3 * NCH * 2;
+  static_assert(HIST_BYTES % 16 == 0, "staged rows must stay 16-byte aligned");
+  __shared__ __align__(16) unsigned char s_hxo[HIST_BYTES + XO_BYTES];
+  auto s_xh = reinterpret_cast<__nv_bfloat16 (*)[NCH]>(s_hxo);
+  auto s_o = reinterpret_cast<float (*)[W]>(s_hxo + HIST_BYTES);  // raw outputs (slab)
   __shared__ float s_w[4][NCH];                         // conv taps of the CTA's channels
   __shared__ __align__(16) float s_dt[kD];              // dt_bias of this head
   __shared__ __align__(16) float s_nw[W];               // norm weight (slab)
@@ -179,7 +184,6 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   __shared__ float2 s_tok[TC];                          // (beta, q_hat . k_hat)
   __shared__ __align__(16) int s_slot[TC];              // checkpoint slot, 0 = none
   __shared__ float s_part[2][CL][TC];                   // CTA r's sum of squares per token (2 chunk buffers)
-  __shared__ __nv_bfloat16 s_hist[3][NCH];              // raw conv history, oldest first (thread-owned)
   __shared__ float2 s_red[ROWSPLIT ? 2 : 1][ROWSPLIT ? NW : 1][ROWSPLIT ? W : 1];  // row form: (a, b) partials
 
   const int rank = CL == 1 ? 0 : (int)(blockIdx.x % CL);
@@ -266,10 +270,10 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
       const __nv_bfloat16* xr = xb + t * a.x_rs + h * kD;
       if (c < 32) {  // q, k sections: all 128 channels
         const int sec = c >> 4, part = c & 15;
-        cp_async16(&s_x[j][sec * kD + part * 8], xr + (int64_t)sec * HD + part * 8);
+        cp_async16(&s_xh[3 + j][sec * kD + part * 8], xr + (int64_t)sec * HD + part * 8);
       } else if (c < 32 + W / 8) {  // v section: this slab
         const int part = c - 32;
-        cp_async16(&s_x[j][2 * kD + part * 8], xr + 2 * (int64_t)HD + slab0 + part * 8);
+        cp_async16(&s_xh[3 + j][2 * kD + part * 8], xr + 2 * (int64_t)HD + slab0 + part * 8);
       } else if (c < 48 + W / 8) {
         const int part = c - 32 - W / 8;
         cp_async16(&s_gr[j][part * 8], gb + t * a.g_rs + (int64_t)h * a.g_hs + part * 8);
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   for (int lc = tid; lc < NCH; lc += NT) {
     const __nv_bfloat16* cp = cs + (int64_t)s0 * a.cs_slot_stride + sec_of(lc) * HD + h * kD + cis_of(lc);
 #pragma unroll
-    for (int p = 0; p < 3; ++p) s_hist[p][lc] = cp[p * a.cs_tap_stride];
+    for (int p = 0; p < 3; ++p) s_xh[p][lc] = cp[p * a.cs_tap_stride];
   }
   // Cluster: every CTA reads the start slot's history of all q and k
   // channels, but writes the checkpoints of its own slab only, and a
@@ -383,59 +387,47 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
       if (tc0 == t0) cluster_wait();  // every peer has read the start slot's conv history
     }
     // ---- A: conv + SiLU and this CTA's share of the conv checkpoints
-    // The raw inputs of a channel, oldest first: its three history taps, then
-    // the chunk's tokens.  Token j's conv reads entries j .. j+3 and leaves
-    // the history j+1 .. j+3, so the chunk's tokens are independent here.
-    for (int lc = tid; lc < NCH; lc += NT) {
-      const int sec = sec_of(lc), cis = cis_of(lc);
-      const int64_t ch = (int64_t)sec * HD + h * kD + cis;
-      const bool owner = cis >= slab0 && cis < slab0 + W;
-      const float w0 = s_w[0][lc], w1 = s_w[1][lc], w2 = s_w[2][lc], w3 = s_w[3][lc];
-      __nv_bfloat16 xr[TC + 3];
-#pragma unroll
-      for (int p = 0; p < 3; ++p) xr[p] = s_hist[p][lc];
-#pragma unroll
-      for (int j = 0; j < TC; ++j) {  // staged rows >= nt are stale: read as zero
-        const __nv_bfloat16 t = s_x[j][lc];
-        xr[3 + j] = j < nt ? t : __float2bfloat16(0.f);
+    // Token j's conv reads raw rows j .. j+3 and leaves the history j+1 ..
+    // j+3, so the chunk's (token, channel) items are independent: they are
+    // spread evenly over the threads, tokens outer, the chunk's nt tokens only.
+    for (int i = tid; i < nt * NCH; i += NT) {
+      const int j = i / NCH, lc = i - j * NCH;
+      float y = s_w[0][lc] * __bfloat162float(s_xh[j][lc]);
+      y = fmaf(s_w[1][lc], __bfloat162float(s_xh[j + 1][lc]), y);
+      y = fmaf(s_w[2][lc], __bfloat162float(s_xh[j + 2][lc]), y);
+      y = fmaf(s_w[3][lc], __bfloat162float(s_xh[j + 3][lc]), y);
+      s_act[j][lc] = y * sigmoid_fast(y);
+      const int cis = cis_of(lc);
+      const int sl = s_slot[j];
+      if (sl != 0 && cis >= slab0 && cis < slab0 + W) {  // this CTA's channels: token j's conv checkpoint
+        __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + (int64_t)sec_of(lc) * HD + h * kD + cis;
+        cp[0] = s_xh[j + 1][lc];
+        cp[a.cs_tap_stride] = s_xh[j + 2][lc];
+        cp[2 * a.cs_tap_stride] = s_xh[j + 3][lc];
       }
-      // All TC rows are computed without branches; rows >= nt are never read.
+    }
+    // The next chunk's history, rows nt .. nt+2, held in registers until
+    // every thread has read this chunk's rows (the barrier below).
+    constexpr int HPT = (NCH + NT - 1) / NT;  // history channels per thread
+    __nv_bfloat16 nh[HPT][3];
 #pragma unroll
-      for (int j = 0; j < TC; ++j) {
-        float y = w0 * __bfloat162float(xr[j]);
-        y = fmaf(w1, __bfloat162float(xr[j + 1]), y);
-        y = fmaf(w2, __bfloat162float(xr[j + 2]), y);
-        y = fmaf(w3, __bfloat162float(xr[j + 3]), y);
-        s_act[j][lc] = y * sigmoid_fast(y);
-      }
-      if (owner) {
-        const int4 sa = *reinterpret_cast<const int4*>(&s_slot[0]);
-        const int4 sb = *reinterpret_cast<const int4*>(&s_slot[4]);
-        const int sls[TC] = {sa.x, sa.y, sa.z, sa.w, sb.x, sb.y, sb.z, sb.w};
+    for (int c = 0; c < HPT; ++c) {
+      const int lc = tid + c * NT;
 #pragma unroll
-        for (int j = 0; j < TC; ++j) {
-          const int sl = j < nt ? sls[j] : 0;
-          if (sl != 0) {
-            __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + ch;
-            cp[0] = xr[j + 1];
-            cp[a.cs_tap_stride] = xr[j + 2];
-            cp[2 * a.cs_tap_stride] = xr[j + 3];
-          }
-        }
-      }
-#pragma unroll
-      for (int p = 0; p < 3; ++p) {
-        __nv_bfloat16 hv = xr[p];
-#pragma unroll
-        for (int q = 1; q <= TC; ++q)
-          if (q == nt) hv = xr[q + p];
-        s_hist[p][lc] = hv;
-      }
+      for (int p = 0; p < 3; ++p) nh[c][p] = lc < NCH ? s_xh[nt + p][lc] : __float2bfloat16(0.f);
     }
     if constexpr (!kLatePrefetch) {
       if (tid == 0 && tc0 == t0) publish_next();
     }
     __syncthreads();
+#pragma unroll
+    for (int c = 0; c < HPT; ++c) {
+      const int lc = tid + c * NT;
+      if (lc < NCH) {
+#pragma unroll
+        for (int p = 0; p < 3; ++p) s_xh[p][lc] = nh[c][p];
+      }
+    }
     if constexpr (!kLatePrefetch) prefetch_next(tc0);
 
     // ---- B: per-token decays and coefficients
