@@ -298,10 +298,12 @@ kda_status kda_set_split_override(int32_t split);
  * "Frozen / speculative-verify mode" names the WY-parallel tensor-core form
  * of these rows): per chunk of up to 8 tokens, S^T [P k | P q] and the
  * rank-T update run as tcgen05 MMAs with float32 accumulators in tensor
- * memory, bf16 high/low operand splits keeping them within ~2^-16 of
- * float32; one persistent CTA per SM.  Forcing MMA with a float32 state
- * returns KDA_ERR_UNSUPPORTED.  The speculative entry points otherwise use
- * SPLIT (one CTA per row, head and value slab, the state in registers).
+ * memory, every operand as three bf16 pieces (within 2^-24 of its float32
+ * value); one persistent CTA per SM.  The dispatcher picks it for a bfloat16
+ * state pool with t_max >= 14 (unless a split or the SPLIT/STREAM schedule is
+ * forced); forcing MMA with a float32 state returns KDA_ERR_UNSUPPORTED.
+ * The speculative entry points otherwise use SPLIT (one CTA per row, head
+ * and value slab, the state in registers).
  */
 typedef enum kda_schedule {
   KDA_SCHED_AUTO = 0,

@@ -265,15 +265,19 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
 //    SM (packed K3 B >= 64), the split kernel below;
 //  - fused: the streaming kernel from five units per SM (H=32 rows=256
 //    fp32: 88 % vs 68 % split; rows=32: 59 % vs 52 %), split below;
-//  - speculative rows: the split kernel.
+//  - speculative rows: the split kernel, except a bfloat16 state with
+//    t_max >= 14, which takes the tensor-core chunked form (N=128, rows of
+//    exactly T tokens: T=14 102.5 vs 129.6 us, T=16 104.6 vs 142.1 us;
+//    ragged rows up to T: 77.0 vs 75.0, 81.1 vs 79.1 us; at T=12 ragged rows
+//    lose 5 % and at T=10 11 %, so below 14 the split kernel stays).
 int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
-  (void)t_max;
   const int forced = g_schedule_override.load();
   if (op == KDA_OP_PACKED_FUSED) return KDA_SCHED_SPLIT;
   if (op == KDA_OP_SPEC) {
+    (void)units; (void)sms;
     if (forced == KDA_SCHED_SPLIT || forced == KDA_SCHED_MMA) return forced;
-    (void)units; (void)sms; (void)state_dtype;
-    return KDA_SCHED_SPLIT;
+    if (forced == KDA_SCHED_STREAM || g_split_override.load() != 0) return KDA_SCHED_SPLIT;
+    return state_dtype == KDA_BF16 && t_max >= 14 ? KDA_SCHED_MMA : KDA_SCHED_SPLIT;
   }
   if (forced == KDA_SCHED_SPLIT || forced == KDA_SCHED_STREAM) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;

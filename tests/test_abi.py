@@ -432,9 +432,18 @@ def test_schedule_override_and_plan(lib):
     assert binding.kda_plan_schedule(2, 8192, 0, 1, 152) == 2  # fused, many units
     assert binding.kda_plan_schedule(2, 1024, 0, 1, 152) == 2
     assert binding.kda_plan_schedule(2, 256, 0, 1, 152) == 1
+    # speculative rows: the tensor-core form for a bf16 state with t_max >= 14
+    assert binding.kda_plan_schedule(3, 2048, 1, 14, 152) == 3
+    assert binding.kda_plan_schedule(3, 2048, 1, 16, 152) == 3
+    assert binding.kda_plan_schedule(3, 2048, 1, 13, 152) == 1
+    assert binding.kda_plan_schedule(3, 2048, 0, 16, 152) == 1  # fp32 state: split kernel
     assert lib.kda_set_split_override(8) == OK  # a forced split implies the split schedule
     assert binding.kda_plan_schedule(1, 6144, 1, 1, 152) == 1
+    assert binding.kda_plan_schedule(3, 2048, 1, 16, 152) == 1
     assert lib.kda_set_split_override(0) == OK
+    assert lib.kda_set_schedule_override(2) == OK
+    assert binding.kda_plan_schedule(3, 2048, 1, 16, 152) == 1  # stream does not apply to spec rows
+    assert lib.kda_set_schedule_override(0) == OK
     assert binding.kda_plan_schedule(9, 6144, 1, 1, 152) == 0
 
 

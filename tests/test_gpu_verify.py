@@ -243,13 +243,22 @@ def test_verify_no_rows_all_token_rows_padding():
     assert torch.isnan(corr).all() and torch.isnan(kg).all()
 
 
-@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
-def test_verify_full_size(state_dtype):
-    """N=128 rows of up to 16 tokens (H=16) from a read-only pool of either dtype."""
+@pytest.mark.parametrize("state_dtype,schedule", [(torch.float32, binding.SCHED_AUTO),
+                                                  (torch.bfloat16, binding.SCHED_AUTO),
+                                                  (torch.bfloat16, binding.SCHED_SPLIT)])
+def test_verify_full_size(state_dtype, schedule):
+    """N=128 rows of up to 16 tokens (H=16) from a read-only pool of either
+    dtype; with a bf16 pool the dispatcher's choice at t_max=16 (the
+    tensor-core form) and the per-token kernel."""
     case = synth.spec_case(128, 16, seed=22, null_count=8, state_dtype=state_dtype)
     d = P.to_device(case)
     before = d["state"].clone()
     corr, kg = _caches(case["state"].shape[0], 16, 16)
-    out = _run(d, 16, corr, kg)
-    torch.cuda.synchronize()
+    binding.kda_set_schedule_override(schedule)
+    try:
+        out = _run(d, 16, corr, kg)
+        torch.cuda.synchronize()
+    finally:
+        binding.kda_set_schedule_override(binding.SCHED_AUTO)
     _check(case, d, before, out, corr, kg, 16)
+    assert binding.kda_device_error() == 0
