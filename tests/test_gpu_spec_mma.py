@@ -197,3 +197,13 @@ def test_mma_verify_then_decode_agree(mma):
     out_d = TS._run(d, 6)
     torch.cuda.synchronize()
     assert torch.equal(out_v, out_d)
+
+
+def test_auto_schedule_takes_the_tensor_core_form_for_long_bf16_rows():
+    """With a bf16 pool and t_max >= 14 the dispatcher picks the tensor-core
+    form on its own; the rows (two chunks each, some ragged) match the
+    oracle like the forced schedule does."""
+    assert binding.kda_plan_schedule(binding.OP_SPEC, 20 * 4, 1, 16, 152) == binding.SCHED_MMA
+    assert binding.kda_plan_schedule(binding.OP_SPEC, 20 * 4, 1, 13, 152) == binding.SCHED_SPLIT
+    case = synth.spec_case(20, 16, seed=341, H=4, null_count=2, state_dtype=BF16)
+    _spec(case, 16)
