@@ -194,15 +194,20 @@ def test_spec_no_rows_all_token_rows_padding():
     assert torch.equal(before, d["state"])
 
 
-@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
-def test_spec_full_size_every_row(state_dtype):
-    """The timed size (N=128, T <= 6, H=16) with either state dtype: every
-    token row and every live slot against the oracle."""
-    case = synth.spec_case(128, 6, seed=21, null_count=8, state_dtype=state_dtype)
+@pytest.mark.parametrize("state_dtype,t_max,fixed", [(torch.float32, 6, False), (torch.bfloat16, 6, False),
+                                                     (torch.bfloat16, 16, False), (torch.bfloat16, 16, True)])
+def test_spec_full_size_every_row(state_dtype, t_max, fixed):
+    """The timed size (N=128, T <= 6, H=16) with either state dtype, and with
+    a bf16 pool rows of up to and of exactly 16 tokens (the dispatcher's
+    tensor-core form, two chunks a row): every token row and every live slot
+    against the oracle."""
+    case = synth.spec_case(128, t_max, seed=21, null_count=8, state_dtype=state_dtype,
+                           lengths=[t_max] * 128 if fixed else None)
     d = P.to_device(case)
     before = d["state"].clone()
     out = torch.full(case["q"].shape, float("nan"), dtype=torch.bfloat16, device="cuda")
-    _run(d, 6, out=out)
+    _run(d, t_max, out=out)
     torch.cuda.synchronize()
     assert not torch.isnan(out).any()
     _check(case, d, before, out)
+    assert binding.kda_device_error() == 0
