@@ -662,19 +662,24 @@ def path_measurements(flush, peak):
     for B in (1, 8, 16, 31, 32, 64, 128, 256, 512):
         n = max(1, min(16, 2047 // B))
         run(Packed(B=B, slots=2048, n_sets=n, seed=B), n)
+    # Small batches replay up to 16 calls per graph on distinct slot sets, as
+    # the T=1 paths above do, so that the graph's own launch is spread over
+    # the calls it holds.
     for H, rows in ((8, 1), (8, 32), (8, 256), (12, 256), (32, 32), (32, 256), (96, 256)):
-        n = max(1, min(16, (2 * rows) // max(rows, 1)))
-        run(Fused(H=H, rows=rows, n_sets=n, seed=H + rows), n)
+        n = min(16, max(2, 1024 // rows))
+        run(Fused(H=H, rows=rows, slots=n * rows + 1, n_sets=n, seed=H + rows), n)
     for N, T in ((1, 6), (16, 6), (128, 2), (128, 4), (128, 6)):
-        run(Spec(N=N, t_max=T, H=16, n_sets=2, seed=N + T), 2)
+        n = 16 if N <= 16 else 2
+        run(Spec(N=N, t_max=T, H=16, slots=max(4 * N, n * N + 1), n_sets=n, seed=N + T), n)
     # bf16 state: the per-token kernel (the policy's choice) and the tensor-core
     # chunked form, on ragged rows and on rows of exactly T tokens
     for N, T, fixed in ((128, 6, False), (128, 6, True), (128, 8, True), (128, 16, True)):
         for sched in (None, binding.SCHED_MMA):
             run(Spec(N=N, t_max=T, H=16, state_dtype=torch.bfloat16, n_sets=2, seed=N + T, fixed=fixed), 2, sched)
     for H, N in ((12, 1), (12, 8), (12, 32), (12, 128), (24, 8), (24, 128)):
+        n = 16 if N <= 8 else 2
         for dt in (torch.float32, torch.bfloat16):
-            run(PackedFused(N=N, T=5, H=H, state_dtype=dt, n_sets=2, seed=H + N), 2)
+            run(PackedFused(N=N, T=5, H=H, state_dtype=dt, n_sets=n, seed=H + N), n)
     torch.cuda.empty_cache()
     return res
 
