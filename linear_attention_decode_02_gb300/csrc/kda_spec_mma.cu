@@ -46,6 +46,8 @@
 // bounded in time: a role whose wait times out records a bit in the error
 // word, raises the CTA's abort flag and leaves its loop; every role then
 // meets at the final barrier before the tensor memory is freed.
+#include <atomic>
+
 #include "kda_stream_common.cuh"
 #include "kda_tcgen05.cuh"
 
@@ -730,14 +732,14 @@ template <bool VERIFY>
 cudaError_t launch_spec_mma_variant(const SpecArgs& a, int sm_count, cudaStream_t s) {
   CUtensorMap map;
   if (!encode_state_map<__nv_bfloat16>(&map, a.state, a.H, a.num_slots, a.slot_stride)) return cudaErrorNotSupported;
-  static bool set[64] = {};
+  static std::atomic<bool> set[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !set[dev]) {
+  if (dev >= 0 && dev < 64 && !set[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kda_spec_mma_kernel<VERIFY>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)MMA_SMEM);
     if (e != cudaSuccess) return e;
-    set[dev] = true;
+    set[dev].store(true, std::memory_order_release);
   }
   const int64_t units = (int64_t)a.N * a.H;
   const int grid = (int)(units < sm_count ? (units > 0 ? units : 1) : sm_count);

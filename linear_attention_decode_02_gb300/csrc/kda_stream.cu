@@ -22,6 +22,8 @@
 // times out records a bit in g_kda_device_error and leaves.  The only
 // barrier spanning warps after set-up (fused RMSNorm) is an AND vote, so
 // the consumers leave together instead of waiting on a departed warp.
+#include <atomic>
+
 #include "kda_stream_common.cuh"
 
 namespace kda {
@@ -562,14 +564,15 @@ __global__ void kda_selftest_wait_kernel() {
 namespace {
 
 template <typename Kernel>
-cudaError_t ensure_smem(Kernel k, size_t bytes, bool* set_flags) {
+cudaError_t ensure_smem(Kernel k, size_t bytes, std::atomic<bool>* set_flags) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < 64 && !set_flags[dev]) {
+  if (dev >= 0 && dev < 64 && !set_flags[dev].load(std::memory_order_acquire)) {
+    // idempotent, so two host threads that both get here set the same value
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
-    set_flags[dev] = true;
+    set_flags[dev].store(true, std::memory_order_release);
   }
   return cudaSuccess;
 }
@@ -578,7 +581,7 @@ template <typename StateT, int PARTS>
 cudaError_t launch_t1_stream_typed(const T1Args& a, int sm_count, cudaStream_t s) {
   CUtensorMap map;
   if (!encode_state_map<StateT>(&map, a.state, a.H, a.num_slots, a.slot_stride)) return cudaErrorNotSupported;
-  static bool set[64] = {};
+  static std::atomic<bool> set[64];
   constexpr size_t smem = t1_stream_smem<StateT, PARTS>();
   cudaError_t e = ensure_smem(kda_t1_stream_kernel<StateT, PARTS>, smem, set);
   if (e != cudaSuccess) return e;
@@ -592,7 +595,7 @@ template <typename StateT>
 cudaError_t launch_fused_stream_typed(const FusedArgs& a, int sm_count, cudaStream_t s) {
   CUtensorMap map;
   if (!encode_state_map<StateT>(&map, a.state, a.H, a.num_slots, a.slot_stride)) return cudaErrorNotSupported;
-  static bool set[64] = {};
+  static std::atomic<bool> set[64];
   constexpr size_t smem = fused_stream_smem<StateT>();
   cudaError_t e = ensure_smem(kda_fused_stream_kernel<StateT>, smem, set);
   if (e != cudaSuccess) return e;
