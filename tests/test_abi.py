@@ -449,3 +449,31 @@ def test_schedule_override_and_plan(lib):
 
 def test_device_error_query_needs_a_pointer(lib):
     assert lib.kda_device_error(None, 0) == INVALID
+
+
+def test_error_messages_are_per_thread(lib):
+    """Two host threads make failing calls at the same time (ctypes releases
+    the GIL for the call): each reads back only its own call's message."""
+    import threading
+
+    null_args = [None] * 10
+    t = binding.KdaTensor()
+    t.ndim = 0
+    rank0_args = [ctypes.byref(t)] * 10
+    failures = []
+
+    def worker(args, expect):
+        for _ in range(2000):
+            st = lib.kda_recurrent_decode(*args, 0, 0.0, 0.088, None)
+            msg = lib.kda_last_error_message().decode()
+            if st != INVALID or expect not in msg:
+                failures.append((st, msg))
+                return
+
+    threads = [threading.Thread(target=worker, args=(null_args, "null tensor descriptor")),
+               threading.Thread(target=worker, args=(rank0_args, "ndim 0"))]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not failures, failures[:3]

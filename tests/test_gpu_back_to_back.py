@@ -139,3 +139,51 @@ def test_packed_fused_back_to_back(graph, cluster):
                  graph)
     finally:
         binding.kda_set_split_override(0)
+
+
+def test_concurrent_host_threads_on_their_own_streams():
+    """Two host threads drive the library at once, each on its own stream with
+    its own state pool (chains of dependent recurrent and speculative calls):
+    both end exactly where the same calls run one after another end."""
+    import threading
+
+    def make(seed):
+        rc = synth.recurrent_case(8, 4, 32, seed=seed, state_dtype=torch.bfloat16)
+        sc = synth.spec_case(6, 4, seed=seed + 1, H=4, state_dtype=torch.bfloat16)
+        return P.to_device(rc), P.to_device(sc)
+
+    def chain(dr, ds, reps):
+        for _ in range(reps):
+            TR._run_recurrent(dr)
+            TS._run(ds, 4)
+
+    cases = [make(601), make(611)]
+    init = [(dr["state"].clone(), ds["state"].clone()) for dr, ds in cases]
+    for dr, ds in cases:
+        chain(dr, ds, 20)
+    torch.cuda.synchronize()
+    ref = [(dr["state"].clone(), ds["state"].clone()) for dr, ds in cases]
+    for (dr, ds), (s_r, s_s) in zip(cases, init):
+        dr["state"].copy_(s_r)
+        ds["state"].copy_(s_s)
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            st = torch.cuda.Stream()
+            with torch.cuda.stream(st):
+                chain(*cases[i], 20)
+            st.synchronize()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    for (dr, ds), (r_r, r_s) in zip(cases, ref):
+        assert torch.equal(dr["state"], r_r) and torch.equal(ds["state"], r_s)
