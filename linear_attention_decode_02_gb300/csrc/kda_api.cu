@@ -294,19 +294,21 @@ bool rows_aligned16(const View& v) {
   return true;
 }
 
-// Packed fused speculative decode: CTAs per (sequence, head) cluster.
-// A cluster spreads a unit's checkpoint stores over its SMs but repeats the
-// conv and coefficient phases in every CTA, so the widest cluster whose CTAs
-// all fit one per SM wins.  Measured on GB300 (T=5, CUDA-graph replays after
-// an L2 flush), fp32 state: H=12 N=1 12.5 us at 8 CTAs (15.6 at 1); H=12 N=2
-// and H=24 N=1 13.8 / 13.5 us at 4 (15.6 / 15.4 at 1); H=12 N=4 15.1 us at
-// 2 (16.5 at 1); from H=12 N=8 up one CTA per unit.  With a bf16 state the
-// 4-CTA row form is slower than 2 CTAs (H=12 N=1: 16.6 vs 14.5 us), so bf16
-// goes from 8 straight to 2 (H=12 N=2: 14.4 vs 14.9 us at 1).
+// Packed fused speculative decode: CTAs per (sequence, head) cluster.  A
+// cluster spreads a unit's conv, checkpoint stores and token updates over
+// its SMs (each CTA convolves its own slab of q, k and v and shares its q
+// and k activations through distributed shared memory) but repeats the
+// coefficient phase, and the row forms (4 and 8 CTAs) pay a CTA barrier per
+// token.  Measured on GB300 (H=12, T=5, CUDA-graph replays of 16 calls after
+// an L2 flush, us at 1 / 2 / 4 / 8 CTAs): fp32 N=1 12.6 / 11.6 / 9.9 / 11.2,
+// N=2 12.9 / 11.9 / 10.3 / 11.7, N=3 13.0 / 12.0 / 14.1 / 12.2, N=4
+// 13.0 / 13.6 / 14.7 / 19.4; bf16 N=1 11.1 / 11.1 / 13.1 / 12.8, N=3
+// 11.3 / 11.3 / 19.6 / 15.5, N=4 11.4 / 12.4 / 20.2 / 21.7.  So fp32 takes 4
+// CTAs while 6 units <= SMs and 2 while 4 units <= SMs, bf16 2 while 4
+// units <= SMs; otherwise one persistent CTA per unit.
 int plan_cluster(int64_t units, int state_dtype, int sms) {
-  if (8 * units <= sms) return 8;
-  if (state_dtype == KDA_F32 && 4 * units <= sms) return 4;
-  return 2 * units <= sms ? 2 : 1;
+  if (state_dtype == KDA_F32 && 6 * units <= sms) return 4;
+  return 4 * units <= sms ? 2 : 1;
 }
 
 int plan_split(int op, int64_t units, int state_dtype, int t_max, int sms) {

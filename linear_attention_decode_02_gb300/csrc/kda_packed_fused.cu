@@ -153,8 +153,9 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   constexpr int NT = NW * 32, TC = 8;
   constexpr int CL = kD / W;                 // CTAs per (sequence, head)
   constexpr int CW = ROWSPLIT ? W : W / NW;  // columns of one warp's strip
-  constexpr int NCH = 2 * kD + W;  // conv channels: all of q and k, this slab of v
-  constexpr int PT = 48 + W / 4;   // 16-byte staging pieces per token
+  constexpr int NCH = 2 * kD + W;  // activations a CTA needs: all of q and k, this slab of v
+  constexpr int NCV = 3 * W;       // conv channels a CTA computes: this slab of q, of k and of v
+  constexpr int PT = W / 2 + 16;   // 16-byte staging pieces per token: the three slabs, the gate
   using G = Strip<StateT, CW>;
   // fragments per lane: all 128 rows (column form) or the warp's 16 (row form)
   constexpr int P = ROWSPLIT ? (kD / NW) / G::RPI : G::PASSES;
@@ -167,13 +168,13 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   // The conv's raw inputs of a channel in one column, oldest first: rows 0-2
   // the history, rows 3 .. 3 + nt - 1 the staged chunk rows (q | k | v slab).
   // The raw outputs (phase C) reuse the staged rows, never the history.
-  constexpr int XO_BYTES = TC * NCH * 2 > TC * W * 4 ? TC * NCH * 2 : TC * W * 4;
-  constexpr int HIST_BYTES = 3 * NCH * 2;
+  constexpr int XO_BYTES = TC * NCV * 2 > TC * W * 4 ? TC * NCV * 2 : TC * W * 4;
+  constexpr int HIST_BYTES = 3 * NCV * 2;
   static_assert(HIST_BYTES % 16 == 0, "staged rows must stay 16-byte aligned");
   __shared__ __align__(16) unsigned char s_hxo[HIST_BYTES + XO_BYTES];
-  auto s_xh = reinterpret_cast<__nv_bfloat16 (*)[NCH]>(s_hxo);
+  auto s_xh = reinterpret_cast<__nv_bfloat16 (*)[NCV]>(s_hxo);
   auto s_o = reinterpret_cast<float (*)[W]>(s_hxo + HIST_BYTES);  // raw outputs (slab)
-  __shared__ float s_w[4][NCH];                         // conv taps of the CTA's channels
+  __shared__ float s_w[4][NCV];                         // conv taps of the CTA's channels
   __shared__ __align__(16) float s_dt[kD];              // dt_bias of this head
   __shared__ __align__(16) float s_nw[W];               // norm weight (slab)
   __shared__ __align__(16) __nv_bfloat16 s_gr[TC][kD];  // staged raw gates
@@ -195,9 +196,11 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   const int col0 = slab0 + lcol;
   const int row0 = (ROWSPLIT ? warp * (kD / NW) : 0) + lane / G::LPR;   // rows row0 + i*RPI, i < P
   const int HD = a.H * kD;
-  // Section and channel-within-section of local conv channel lc.
-  auto sec_of = [](int lc) { return lc < kD ? 0 : (lc < 2 * kD ? 1 : 2); };
-  auto cis_of = [slab0](int lc) { return lc < 2 * kD ? (lc & (kD - 1)) : slab0 + lc - 2 * kD; };
+  // Local conv channel lc (this CTA's slab of q, then of k, then of v): its
+  // section, its channel within the section and its column of s_act.
+  auto sec_of = [](int lc) { return lc / W; };
+  auto cis_of = [slab0](int lc) { return slab0 + lc % W; };
+  auto act_of = [slab0](int lc) { return lc < 2 * W ? (lc / W) * kD + slab0 + lc % W : 2 * kD + lc - 2 * W; };
   __shared__ int4 s_pf;  // next unit: (start slot or 0, first token, end token, head)
   pdl_wait();
   pdl_launch_dependents();
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
 
   // Parameters first: they depend on nothing, so their copies overlap the
   // metadata loads below.
-  for (int lc = tid; lc < NCH; lc += NT) {
+  for (int lc = tid; lc < NCV; lc += NT) {
     const float* w = a.conv_w + (int64_t)sec_of(lc) * 4 * HD + h * kD + cis_of(lc);
 #pragma unroll
     for (int p = 0; p < 4; ++p) cp_async4(&s_w[p][lc], w + (int64_t)p * HD);
@@ -268,17 +271,14 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
       const int j = i / PT, c = i % PT;
       const int64_t t = tc0 + j;
       const __nv_bfloat16* xr = xb + t * a.x_rs + h * kD;
-      if (c < 32) {  // q, k sections: all 128 channels
-        const int sec = c >> 4, part = c & 15;
-        cp_async16(&s_xh[3 + j][sec * kD + part * 8], xr + (int64_t)sec * HD + part * 8);
-      } else if (c < 32 + W / 8) {  // v section: this slab
-        const int part = c - 32;
-        cp_async16(&s_xh[3 + j][2 * kD + part * 8], xr + 2 * (int64_t)HD + slab0 + part * 8);
-      } else if (c < 48 + W / 8) {
-        const int part = c - 32 - W / 8;
+      if (c < 3 * W / 8) {  // the q, k and v sections: this slab of each
+        const int sec = c / (W / 8), part = c % (W / 8);
+        cp_async16(&s_xh[3 + j][sec * W + part * 8], xr + (int64_t)sec * HD + slab0 + part * 8);
+      } else if (c < 3 * W / 8 + 16) {
+        const int part = c - 3 * W / 8;
         cp_async16(&s_gr[j][part * 8], gb + t * a.g_rs + (int64_t)h * a.g_hs + part * 8);
       } else {
-        const int part = c - 48 - W / 8;
+        const int part = c - 3 * W / 8 - 16;
         cp_async16(&s_og[j][part * 8], ogb + t * a.og_rs + (int64_t)h * a.og_hs + slab0 + part * 8);
       }
     }
@@ -310,17 +310,15 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
   }
 
   __nv_bfloat16* cs = static_cast<__nv_bfloat16*>(a.conv_state);
-  for (int lc = tid; lc < NCH; lc += NT) {
+  for (int lc = tid; lc < NCV; lc += NT) {
     const __nv_bfloat16* cp = cs + (int64_t)s0 * a.cs_slot_stride + sec_of(lc) * HD + h * kD + cis_of(lc);
 #pragma unroll
     for (int p = 0; p < 3; ++p) s_xh[p][lc] = cp[p * a.cs_tap_stride];
   }
-  // Cluster: every CTA reads the start slot's history of all q and k
-  // channels, but writes the checkpoints of its own slab only, and a
-  // checkpoint slot may be the start slot itself.  This arrive, with the wait
-  // before the first checkpoint store, orders every CTA's history reads
-  // before any peer's stores; it also guarantees that every CTA of the
-  // cluster is running before the first distributed-shared-memory store.
+  // Cluster: a CTA reads and writes the conv cache of its own slab of each
+  // section only; its q and k activations go to every peer's shared memory.
+  // This arrive, with the wait before phase A, has every CTA of the cluster
+  // running before the first distributed-shared-memory store.
   if constexpr (CL > 1) cluster_arrive();
 
   // The next unit this CTA runs, for its L2 prefetch: its start slot (loaded
@@ -384,23 +382,37 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     if (tid == 0 && tc0 == t0 && next_n < a.N && pf_t1 > pf_t0 && pf_acc >= 1 && pf_acc <= a.cols)
       pf_slot = __ldg(a.idx + (int64_t)next_n * a.idx_rs + pf_acc - 1);
     if constexpr (CL > 1) {
-      if (tc0 == t0) cluster_wait();  // every peer has read the start slot's conv history
+      if (tc0 == t0) cluster_wait();  // every peer is running
     }
-    // ---- A: conv + SiLU and this CTA's share of the conv checkpoints
+    // ---- A: conv + SiLU and the conv checkpoints of this CTA's channels
     // Token j's conv reads raw rows j .. j+3 and leaves the history j+1 ..
     // j+3, so the chunk's (token, channel) items are independent: they are
-    // spread evenly over the threads, tokens outer, the chunk's nt tokens only.
-    for (int i = tid; i < nt * NCH; i += NT) {
-      const int j = i / NCH, lc = i - j * NCH;
+    // spread evenly over the threads, tokens outer, the chunk's nt tokens
+    // only.  In a cluster each q and k activation is written into every
+    // CTA's s_act (its own included); the cluster barrier ending the phase
+    // makes them visible.  A peer's reads of the previous chunk's
+    // activations all precede the previous chunk's RMSNorm cluster barrier.
+    for (int i = tid; i < nt * NCV; i += NT) {
+      const int j = i / NCV, lc = i - j * NCV;
       float y = s_w[0][lc] * __bfloat162float(s_xh[j][lc]);
       y = fmaf(s_w[1][lc], __bfloat162float(s_xh[j + 1][lc]), y);
       y = fmaf(s_w[2][lc], __bfloat162float(s_xh[j + 2][lc]), y);
       y = fmaf(s_w[3][lc], __bfloat162float(s_xh[j + 3][lc]), y);
-      s_act[j][lc] = y * sigmoid_fast(y);
-      const int cis = cis_of(lc);
+      const float act = y * sigmoid_fast(y);
+      const int ac = act_of(lc);
+      if constexpr (CL > 1) {
+        if (lc < 2 * W) {
+#pragma unroll
+          for (int r = 0; r < CL; ++r) *cg::this_cluster().map_shared_rank(&s_act[j][ac], r) = act;
+        } else {
+          s_act[j][ac] = act;
+        }
+      } else {
+        s_act[j][ac] = act;
+      }
       const int sl = s_slot[j];
-      if (sl != 0 && cis >= slab0 && cis < slab0 + W) {  // this CTA's channels: token j's conv checkpoint
-        __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + (int64_t)sec_of(lc) * HD + h * kD + cis;
+      if (sl != 0) {  // token j's conv checkpoint of this channel
+        __nv_bfloat16* cp = cs + (int64_t)sl * a.cs_slot_stride + (int64_t)sec_of(lc) * HD + h * kD + cis_of(lc);
         cp[0] = s_xh[j + 1][lc];
         cp[a.cs_tap_stride] = s_xh[j + 2][lc];
         cp[2 * a.cs_tap_stride] = s_xh[j + 3][lc];
@@ -408,22 +420,27 @@ __global__ void __launch_bounds__(NW * 32, MinBlocks<NW>::value) kda_packed_fuse
     }
     // The next chunk's history, rows nt .. nt+2, held in registers until
     // every thread has read this chunk's rows (the barrier below).
-    constexpr int HPT = (NCH + NT - 1) / NT;  // history channels per thread
+    constexpr int HPT = (NCV + NT - 1) / NT;  // history channels per thread
     __nv_bfloat16 nh[HPT][3];
 #pragma unroll
     for (int c = 0; c < HPT; ++c) {
       const int lc = tid + c * NT;
 #pragma unroll
-      for (int p = 0; p < 3; ++p) nh[c][p] = lc < NCH ? s_xh[nt + p][lc] : __float2bfloat16(0.f);
+      for (int p = 0; p < 3; ++p) nh[c][p] = lc < NCV ? s_xh[nt + p][lc] : __float2bfloat16(0.f);
     }
     if constexpr (!kLatePrefetch) {
       if (tid == 0 && tc0 == t0) publish_next();
     }
-    __syncthreads();
+    if constexpr (CL > 1) {
+      cluster_arrive();  // this CTA's activations are written (release) ...
+      cluster_wait();    // ... and every peer's (acquire)
+    } else {
+      __syncthreads();
+    }
 #pragma unroll
     for (int c = 0; c < HPT; ++c) {
       const int lc = tid + c * NT;
-      if (lc < NCH) {
+      if (lc < NCV) {
 #pragma unroll
         for (int p = 0; p < 3; ++p) s_xh[p][lc] = nh[c][p];
       }

@@ -394,18 +394,15 @@ def test_packed_fused_contract(lib):
 
 
 def test_packed_fused_cluster_policy(lib):
-    # the widest cluster whose CTAs fit one per SM: 8, then 4 (fp32 only), 2, 1
-    assert binding.kda_plan_split(4, 12, 0, 1, 152) == 8
-    assert binding.kda_plan_split(4, 19, 0, 1, 152) == 8
-    assert binding.kda_plan_split(4, 19, 1, 1, 152) == 8
-    assert binding.kda_plan_split(4, 20, 0, 1, 152) == 4
-    assert binding.kda_plan_split(4, 38, 0, 1, 152) == 4
-    assert binding.kda_plan_split(4, 20, 1, 1, 152) == 2
-    assert binding.kda_plan_split(4, 39, 0, 1, 152) == 2
-    assert binding.kda_plan_split(4, 76, 0, 1, 152) == 2
-    assert binding.kda_plan_split(4, 76, 1, 1, 152) == 2
-    assert binding.kda_plan_split(4, 77, 0, 1, 152) == 1
-    assert binding.kda_plan_split(4, 77, 1, 1, 152) == 1
+    # measured policy: fp32 4 CTAs at the smallest batches, then 2, then 1; bf16 2, then 1 (8 only when forced)
+    assert binding.kda_plan_split(4, 12, 0, 1, 152) == 4  # fp32: 4 CTAs while 6 units <= SMs
+    assert binding.kda_plan_split(4, 25, 0, 1, 152) == 4
+    assert binding.kda_plan_split(4, 26, 0, 1, 152) == 2  # then 2 while 4 units <= SMs
+    assert binding.kda_plan_split(4, 38, 0, 1, 152) == 2
+    assert binding.kda_plan_split(4, 39, 0, 1, 152) == 1
+    assert binding.kda_plan_split(4, 12, 1, 1, 152) == 2  # bf16: 2 while 4 units <= SMs
+    assert binding.kda_plan_split(4, 38, 1, 1, 152) == 2
+    assert binding.kda_plan_split(4, 39, 1, 1, 152) == 1
     assert binding.kda_plan_split(4, 96, 0, 1, 152) == 1
     assert binding.kda_plan_split(4, 1536, 1, 1, 152) == 1
     assert binding.kda_plan_schedule(4, 12, 0, 1, 152) == 1
