@@ -114,7 +114,8 @@ __device__ __forceinline__ float strip_reduce_scatter(const float2 (&a2)[G::VEC 
 // token; every CTA keeps 8 warps for the conv and coefficient phases while
 // each SM stores only W/128 of the state.  The per-row coefficients a
 // token's reduction reads, (d k_hat, d q_hat), and those its update reads,
-// (d, k_hat), sit in two arrays of pairs: one 8-byte shared load each.  The state slab is loaded once from the start slot (the
+// (d, k_hat), sit in two arrays of pairs: one 8-byte shared load each.
+// The state slab is loaded once from the start slot (the
 // checkpoint of the last accepted token) and carried in float32 registers
 // across the sequence's tokens; after each token it is stored to that
 // token's checkpoint slot (rounded once if bf16), so a call moves one state
@@ -124,16 +125,18 @@ __device__ __forceinline__ float strip_reduce_scatter(const float2 (&a2)[G::VEC 
 // (conv taps, dt_bias, norm weight) are copied to shared memory
 // asynchronously at entry, alongside the metadata loads (token range,
 // accepted count, the first chunk's checkpoint slots); the chunk's
-// activation rows (the q and k sections of x and this CTA's slab of its v
-// section, the raw gate, this slab of the output gate: 16-byte pieces) are
-// staged as soon as the token range is known, alongside the start-slot
-// lookup; then the state slab and the conv history are loaded.
+// activation rows (this CTA's slab of each of x's q, k and v sections, the
+// raw gate, this slab of the output gate: 16-byte pieces) are staged as
+// soon as the token range is known, alongside the start-slot lookup; then
+// the state slab and the conv history of the CTA's channels are loaded.
 //
 // Tokens go in chunks of up to TC:
-//  A. conv + SiLU of the chunk's tokens for the CTA's 256 + W channels (the
-//     tokens of a channel are independent given its raw inputs; a CTA writes
-//     the conv checkpoints of its slab of each section, so every channel is
-//     written once per cluster);
+//  A. conv + SiLU of the chunk's tokens for the CTA's 3 W channels (its slab
+//     of q, of k and of v; the tokens of a channel are independent given its
+//     raw inputs) and their conv checkpoints, so every channel is computed
+//     and written once per cluster; in a cluster the q and k activations go
+//     to every CTA through distributed shared memory, and a cluster barrier
+//     ends the phase;
 //  B. the warps normalise q, k of the chunk's tokens, form the decays and
 //     write the per-row coefficients (all 128 key rows, in every CTA);
 //  C. every warp runs the chunk's tokens on its strip (column form: no CTA
