@@ -324,12 +324,23 @@ def source_closure(name):
     return sorted(seen)
 
 
+_COMMENT = re.compile(r'//[^\n]*|/\*.*?\*/|"(?:\\.|[^"\\])*"', re.S)
+
+
+def code_only(text):
+    """C++ source without its comments and with whitespace runs collapsed
+    (string literals kept), so that editing a comment leaves the hash alone."""
+    text = _COMMENT.sub(lambda m: m.group(0) if m.group(0).startswith('"') else " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(name="kda_t1.cu"):
-    """Hash of one kernel translation unit and the csrc headers it includes."""
+    """Hash of one kernel translation unit and the csrc headers it includes,
+    comments and whitespace ignored."""
     h = hashlib.sha256()
     for f in source_closure(name):
-        with open(os.path.join(CSRC, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(CSRC, f)) as fh:
+            h.update(f.encode() + b"\0" + code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -60,3 +60,10 @@ def test_oracle_baseline_runs_on_several_single_threaded_processes():
     assert g1 > 0 and r1 >= 8 and e1 >= 0.2
     for g, r, e in per_step:
         assert g > 0 and r >= 16 and e >= 0.2
+
+
+def test_source_hash_ignores_comments_but_not_code():
+    src = 'int f(int x) {  // doubles\n  /* see\n below */ return 2 * x; }\nconst char* s = "// kept";\n'
+    assert bench.code_only(src) == bench.code_only(src.replace("// doubles", "// twice").replace("see", "look"))
+    assert bench.code_only(src) != bench.code_only(src.replace("2 * x", "3 * x"))
+    assert '"// kept"' in bench.code_only(src)
