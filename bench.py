@@ -115,11 +115,11 @@ def _slot_sets(n_sets, count, num_slots, null_count, seed, null_values=(-1,)):
 SPLIT_SOURCE = {0: "kda_t1.cu", 1: "kda_t1.cu", 2: "kda_fused.cu", 3: "kda_spec.cu"}
 
 
-def kernel_source(op, units, state_dtype):
+def kernel_source(op, units, state_dtype, t_max=1):
     """Translation unit of the kernel the library's dispatch picks for this call shape."""
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     code = 0 if state_dtype == torch.float32 else 1
-    sched = binding.kda_plan_schedule(op, units, code, 1, sms)
+    sched = binding.kda_plan_schedule(op, units, code, t_max, sms)
     if sched == binding.SCHED_STREAM:
         return "kda_stream.cu"
     if sched == binding.SCHED_MMA:
@@ -238,7 +238,7 @@ class Spec(Workload):
                            empty_rows=N - live_rows, num_slots=slots,
                            state="float32" if state_dtype == torch.float32 else "bfloat16",
                            gates="precomputed fp32 log decay in [-5, 0]")
-        self.source = kernel_source(3, N * H, state_dtype)
+        self.source = kernel_source(3, N * H, state_dtype, t_max)
         self.e2e_keys = ("q", "k", "v", "g", "beta", "cu_seqlens")
 
     def call(self, idx):
