@@ -285,17 +285,20 @@ class PackedFused(Workload):
 
 
 def make_workload(args, seed):
+    state_dtype = torch.bfloat16 if args.bf16_state else torch.float32
     if args.workload == "recurrent":
-        return Recurrent(B=args.batch or 512, H=args.heads or 32, slots=args.slots or 1024, seed=seed)
+        return Recurrent(B=args.batch or 512, H=args.heads or 32, slots=args.slots or 1024, state_dtype=state_dtype,
+                         seed=seed)
     if args.workload == "packed":
         return Packed(B=args.batch or 512, slots=args.slots or 2048, seed=seed)
     if args.workload == "fused":
-        return Fused(H=args.heads or 32, rows=args.batch or 256, slots=args.slots or None, seed=seed)
+        return Fused(H=args.heads or 32, rows=args.batch or 256, slots=args.slots or None, state_dtype=state_dtype,
+                     seed=seed)
     if args.workload == "packed_fused":
-        return PackedFused(N=args.batch or 128, T=args.t_max or 5, H=args.heads or 12,
-                           state_dtype=torch.bfloat16 if args.bf16_state else torch.float32, seed=seed)
+        return PackedFused(N=args.batch or 128, T=args.t_max or 5, H=args.heads or 12, state_dtype=state_dtype,
+                           seed=seed)
     return Spec(N=args.batch or 128, t_max=args.t_max or 6, H=args.heads or 16, slots=args.slots, seed=seed,
-                state_dtype=torch.bfloat16 if args.bf16_state else torch.float32, fixed=args.fixed)
+                state_dtype=state_dtype, fixed=args.fixed)
 
 
 # ---- environment -------------------------------------------------------------------
@@ -838,7 +841,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=("recurrent", "packed", "fused", "spec", "packed_fused"),
                     default="recurrent")
-    ap.add_argument("--bf16-state", action="store_true", help="packed_fused, spec: bfloat16 state pool")
+    ap.add_argument("--bf16-state", action="store_true", help="recurrent, fused, packed_fused, spec: bfloat16 state pool (packed always has one)")
     ap.add_argument("--fixed", action="store_true", help="spec: every row exactly --t-max tokens")
     ap.add_argument("--schedule", choices=("auto", "split", "stream", "mma"), default="auto",
                     help="force a kernel schedule (mma: the tensor-core speculative form, bf16 state)")
