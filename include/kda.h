@@ -291,7 +291,7 @@ kda_status kda_set_split_override(int32_t split);
  * blocks (TMA, swizzled) and the unit's activation vectors into
  * shared-memory stages with bulk asynchronous copies while consumer warps
  * update earlier ones; needs every activation head vector (and, fused, the
- * conv-cache slots) 16-byte aligned, otherwise the call uses SPLIT, or
+ * conv-cache slots and conv_weight) 16-byte aligned, otherwise the call uses SPLIT, or
  * returns KDA_ERR_UNSUPPORTED if STREAM is forced.
  * MMA (kda_spec_decode and kda_spec_verify_decode with a bfloat16 state
  * pool): the chunked form of the token loop on the tensor cores ([P1]

@@ -579,10 +579,11 @@ kda_status kda_fused_decode(const kda_tensor* x, const kda_tensor* conv_weight, 
   int sched = plan_schedule(KDA_OP_FUSED, rows * H, S.dtype, 1, dev.sms);
   const bool stream_ok = rows_aligned16(X) && rows_aligned16(G) && rows_aligned16(OG) &&
                          reinterpret_cast<uintptr_t>(C.data) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(W.data) % 16 == 0 &&
                          (C.shape[0] <= 1 || (C.stride[0] * 2) % 16 == 0) && rows * H <= INT32_MAX;
   if (sched == KDA_SCHED_STREAM && !stream_ok) {
     KDA_CHECK(g_schedule_override.load() != KDA_SCHED_STREAM, KDA_ERR_UNSUPPORTED,
-              "stream schedule forced but an activation row or conv-cache slot is not 16-byte aligned");
+              "stream schedule forced but an activation row, a conv-cache slot or conv_weight is not 16-byte aligned");
     sched = KDA_SCHED_SPLIT;
   }
 

@@ -1,27 +1,27 @@
 // Persistent streaming decode kernels: one CTA per SM walks its share of the
-// (row, head) units through a ring of shared-memory stages.
+// (row, head) units through rings of shared-memory stages.
 //
 //   loader warp    per unit: the slot index, beta and A_log; TMA tensor
 //                  copies of the 128 x 128 state block (128-byte swizzled,
 //                  in 128-byte-wide column blocks) and bulk copies of the
-//                  unit's activation vectors, all completing on the stage's
-//                  `full` barrier.
+//                  unit's activation vectors.  T=1: one ring, state and
+//                  activations on the stage's `full` barrier.  Fused: two
+//                  rings, the activations a few units ahead of the state.
 //   prologue warps per unit, once, units dealt round-robin: (fused: the short conv + SiLU of the
-//                  head's 384 channels, and the conv-cache shift written back
-//                  from the stage with bulk stores) the L2 norms,
-//                  gate and decay of the 128 key channels into the stage's
-//                  coefficient array (d k, d q, d, k) and q.k; then `ready`.
+//                  head's 384 channels, the conv-cache shift written back
+//                  from registers) the L2 norms, gate and decay of the 128 key
+//                  channels into the coefficient array (d k, d q, d, k) and
+//                  q.k; then `ready`.
 //   8 consumers    per unit: a 16-column strip over all 128 key rows from
 //                  shared memory: the two k-reductions (in-thread plus xor
 //                  shuffles), u and o, release of the stage (`empty`), the
-//                  update written straight from registers to global; (fused:
-//                  the gated RMSNorm through one named barrier per unit).
+//                  update written straight from registers to global.
+//   epilogue warp  (fused) per unit: the gated RMSNorm of the consumers' o.
 //
-// Three (float32) or five (bfloat16) stages keep ~200 KB of state loads in
-// flight per SM.  Every mbarrier wait is bounded in time; a warp whose wait
-// times out records a bit in g_kda_device_error and leaves.  The only
-// barrier spanning warps after set-up (fused RMSNorm) is an AND vote, so
-// the consumers leave together instead of waiting on a departed warp.
+// The state rings keep 160-200 KB of loads in flight per SM.  Every mbarrier
+// wait is bounded in time; a warp whose wait times out records a bit in
+// g_kda_device_error and leaves, and the warps waiting on it time out in turn.
+// No barrier spans warps after set-up.
 #include <atomic>
 
 #include "kda_stream_common.cuh"
@@ -279,50 +279,75 @@ __global__ void __launch_bounds__((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PART
 // =====================================================================================
 // Fused short conv + SiLU + KDA + gated RMSNorm
 // =====================================================================================
-// Stage activations (bf16 unless noted): x of the head's q|k|v channels
+// Activation entry (bf16 unless noted): x of the head's q|k|v channels
 // (3 x 256 B), the conv cache taps (3 taps x 3 sections x 256 B), the raw
-// gate (256 B), dt_bias (512 B, f32) and the output gate (256 B).
+// gate (256 B), dt_bias (512 B, f32) and the output gate (256 B); then the
+// prologue's results: the coefficients (128 float4) and SiLU(conv) of the
+// 128 v channels (f32); the consumers' o before the norm (f32); and the
+// unit's scalars (slot, beta, A, q.k).
 constexpr uint32_t F_X = 0, F_CS = 768, F_G = 3072, F_DT = 3328, F_OG = 3840, F_ACT = 4096;
-constexpr uint32_t F_DERIVED = 3 * kD * sizeof(float);  // SiLU(conv) of the 384 channels
+constexpr uint32_t F_COEF = F_ACT, F_V = F_COEF + kD * 16, F_O = F_V + kD * 4, F_SCAL = F_O + kD * 4,
+                   F_ENTRY = F_SCAL + 16;
 
+// Two rings: NS state stages (TMA destinations, 1024-byte aligned) and NA
+// activation entries.  The loader fills the entries LA = NA - NS units ahead
+// of the state, so the prologue (conv, decay, coefficients: ~2.5 us a unit
+// on one warp) is done before the unit's state lands and is not part of a
+// state stage's turnaround.  NP prologue warps serve the entries
+// round-robin; NP divides NA, so an entry is always served by the same warp
+// in round order (a parity wait cannot tell a phase from the one two rounds
+// later).  The gated RMSNorm runs on an epilogue warp from the consumers' o
+// in the entry, so the consumer warps never wait on one another.
 template <typename StateT>
-using FusedStream = StageCfg<StateT, F_ACT, sizeof(StateT) == 4 ? 3 : 4, F_DERIVED>;
-// Prologue warps (the short conv dominates their work); NP divides NSTAGE.
-template <typename StateT>
-__host__ __device__ constexpr int fused_np() {
-  return sizeof(StateT) == 4 ? 3 : 2;
-}
+struct FusedRing : SwzCfg<StateT> {
+  static constexpr int NS = sizeof(StateT) == 4 ? 3 : 5;
+  static constexpr int NA = sizeof(StateT) == 4 ? 4 : 8;
+  static constexpr int LA = NA - NS;
+  static constexpr int NP = 2;
+  static constexpr int NW = 8;   // consumer warps
+  static constexpr int CW = 16;  // columns per consumer warp
+  static constexpr int WARPS = NW + 1 + NP + 1;  // consumers, loader, prologue, epilogue
+  static constexpr size_t ACT_OFF = (size_t)NS * SwzCfg<StateT>::STATE_BYTES;
+  static constexpr size_t BAR_OFF = ACT_OFF + (size_t)NA * F_ENTRY;
+  static constexpr size_t TAIL_OFF = BAR_OFF + (size_t)(2 * NS + 4 * NA) * sizeof(uint64_t);
+  static_assert(LA >= 0 && NA % NP == 0 && F_ENTRY % 16 == 0 && NW * CW == kD, "fused ring geometry");
+};
 
 template <typename StateT>
 __host__ __device__ constexpr size_t fused_stream_smem() {
-  return FusedStream<StateT>::TAIL_OFF + 2 * FusedStream<StateT>::NW * sizeof(float) + 1024;
+  return FusedRing<StateT>::TAIL_OFF + 1024;
 }
 
 template <typename StateT>
-__global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT>()) * 32, 1)
+__global__ void __launch_bounds__(FusedRing<StateT>::WARPS * 32, 1)
     kda_fused_stream_kernel(const FusedArgs a, const __grid_constant__ CUtensorMap state_map, const int units) {
-  using C = FusedStream<StateT>;
+  using C = FusedRing<StateT>;
   using G = Strip<StateT, C::CW>;
-  static_assert(fused_stream_smem<StateT>() <= 232448, "stages exceed the 227 KB shared memory of a CTA");
-  static_assert(C::NSTAGE % fused_np<StateT>() == 0, "each stage must be served by one prologue warp");
+  static_assert(fused_stream_smem<StateT>() <= 232448, "rings exceed the 227 KB shared memory of a CTA");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  float4* coef_all = reinterpret_cast<float4*>(smem + C::COEF_OFF);
-  float* conv_all = reinterpret_cast<float*>(smem + C::DERIVED_OFF);
-  int4* scal = reinterpret_cast<int4*>(smem + C::SCAL_OFF);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint64_t* ready = full + C::NSTAGE;
-  uint64_t* empty = ready + C::NSTAGE;
-  float* s_ss = reinterpret_cast<float*>(smem + C::TAIL_OFF);  // [2][NW] RMS partial sums
+  auto entry = [&](int e) { return smem + C::ACT_OFF + (size_t)e * F_ENTRY; };
+  auto scal = [&](int e) { return reinterpret_cast<int4*>(entry(e) + F_SCAL); };
+  uint64_t* sfull = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);  // state landed
+  uint64_t* sempty = sfull + C::NS;                                   // consumers done with the stage
+  uint64_t* afull = sempty + C::NS;                                   // activations landed
+  uint64_t* aready = afull + C::NA;                                   // prologue results written
+  uint64_t* aempty = aready + C::NA;                                  // consumers and epilogue done with it
+  uint64_t* odone = aempty + C::NA;                                   // the unit's o written
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::NSTAGE; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&ready[s], 1);
-      mbar_init(&empty[s], C::NW + 1);  // consumers + the prologue warp (its cache write-back reads the stage)
+    for (int s = 0; s < C::NS; ++s) {
+      mbar_init(&sfull[s], 1);
+      mbar_init(&sempty[s], C::NW);
+    }
+    for (int e = 0; e < C::NA; ++e) {
+      mbar_init(&afull[e], 1);
+      mbar_init(&aready[e], 1);
+      mbar_init(&aempty[e], C::NW + 1);  // the prologue is done reading an entry before it marks it ready
+      mbar_init(&odone[e], C::NW);
     }
     mbar_fence_init();
   }
@@ -335,59 +360,79 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
   const int HD = a.H * kD;
 
   if (warp == C::NW) {
-    // ---------------- loader ----------------
-    for (int j0 = 0; j0 < n_my; j0 += 32) {
-      int slot = -1;
-      float beta = 0.f, A = 0.f;
-      if (j0 + lane < n_my) {
-        const int u = blockIdx.x + (j0 + lane) * P;
-        const int h = u % a.H, r = u / a.H;
-        slot = __ldg(a.idx + r);
-        beta = sigmoidf_(load1(a.beta, (int64_t)r * a.b_rs + (int64_t)h * a.b_hs, KDA_DT_BF16));
-        A = expf(__ldg(a.A_log + h));
-      }
-      const int cnt = min(32, n_my - j0);
-      for (int t = 0; t < cnt; ++t) {
-        const int j = j0 + t;
-        const int s = j % C::NSTAGE;
-        const uint32_t round = j / C::NSTAGE;
-        const int slot_t = __shfl_sync(0xffffffffu, slot, t);
-        const float beta_t = __shfl_sync(0xffffffffu, beta, t);
-        const float A_t = __shfl_sync(0xffffffffu, A, t);
-        const bool ok = round == 0 || mbar_wait(&empty[s], (round - 1) & 1);
+    // ---------------- loader: step k issues unit k's activations and unit k - LA's state ----------------
+    int slot = -1;
+    float beta = 0.f, A = 0.f;
+    for (int k = 0; k < n_my + C::LA; ++k) {
+      if (k < n_my) {
+        if ((k & 31) == 0) {  // slot, beta and A of units k .. k+31, one per lane
+          slot = -1;
+          if (k + lane < n_my) {
+            const int u = blockIdx.x + (k + lane) * P;
+            const int h = u % a.H, r = u / a.H;
+            slot = __ldg(a.idx + r);
+            beta = sigmoidf_(load1(a.beta, (int64_t)r * a.b_rs + (int64_t)h * a.b_hs, KDA_DT_BF16));
+            A = expf(__ldg(a.A_log + h));
+          }
+        }
+        const int slot_t = __shfl_sync(0xffffffffu, slot, k & 31);
+        const float beta_t = __shfl_sync(0xffffffffu, beta, k & 31);
+        const float A_t = __shfl_sync(0xffffffffu, A, k & 31);
+        const int e = k % C::NA;
+        const uint32_t round = k / C::NA;
+        const bool ok = round == 0 || mbar_wait(&aempty[e], (round - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
           if (lane == 0) record_error(2u);
           return;
         }
         if (lane == 0) {
-          const int u = blockIdx.x + j * P;
+          const int u = blockIdx.x + k * P;
           const int h = u % a.H, r = u / a.H;
           const bool live = slot_t > 0 && slot_t < a.num_slots;
-          scal[s] = make_int4(live ? slot_t : -1, __float_as_int(beta_t), __float_as_int(A_t), 0);
+          *scal(e) = make_int4(live ? slot_t : -1, __float_as_int(beta_t), __float_as_int(A_t), 0);
           if (live) {
-            unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
-            unsigned char* act = st + C::STATE_BYTES;
-            mbar_arrive_expect_tx(&full[s], C::STATE_BYTES + F_ACT);
-            tma_load_state<StateT>(st, &state_map, h, slot_t, &full[s]);
+            unsigned char* act = entry(e);
+            mbar_arrive_expect_tx(&afull[e], F_ACT);
             const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(a.x) + (int64_t)r * a.x_rs + h * kD;
             const __nv_bfloat16* cs = static_cast<const __nv_bfloat16*>(a.conv_state) +
                                       (int64_t)slot_t * a.cs_slot_stride + h * kD;
 #pragma unroll
             for (int sec = 0; sec < 3; ++sec) {
-              bulk_load(act + F_X + sec * 256, xr + sec * HD, 256, &full[s]);
+              bulk_load(act + F_X + sec * 256, xr + sec * HD, 256, &afull[e]);
 #pragma unroll
               for (int tap = 0; tap < 3; ++tap)
-                bulk_load(act + F_CS + (tap * 3 + sec) * 256, cs + tap * a.cs_tap_stride + sec * HD, 256, &full[s]);
+                bulk_load(act + F_CS + (tap * 3 + sec) * 256, cs + tap * a.cs_tap_stride + sec * HD, 256, &afull[e]);
             }
             bulk_load(act + F_G,
                       static_cast<const __nv_bfloat16*>(a.gate) + (int64_t)r * a.g_rs + (int64_t)h * a.g_hs, 256,
-                      &full[s]);
-            bulk_load(act + F_DT, a.dt_bias + h * kD, 512, &full[s]);
+                      &afull[e]);
+            bulk_load(act + F_DT, a.dt_bias + h * kD, 512, &afull[e]);
             bulk_load(act + F_OG,
                       static_cast<const __nv_bfloat16*>(a.out_gate) + (int64_t)r * a.og_rs + (int64_t)h * a.og_hs,
-                      256, &full[s]);
+                      256, &afull[e]);
           } else {
-            mbar_arrive(&full[s]);
+            mbar_arrive(&afull[e]);
+          }
+        }
+        __syncwarp();
+      }
+      if (k >= C::LA) {
+        const int js = k - C::LA;
+        const int s = js % C::NS;
+        const uint32_t round = js / C::NS;
+        const bool ok = round == 0 || mbar_wait(&sempty[s], (round - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          if (lane == 0) record_error(2u);
+          return;
+        }
+        if (lane == 0) {
+          const int slot_s = scal(js % C::NA)->x;  // written above by this thread; the entry is not reused yet
+          if (slot_s >= 0) {
+            mbar_arrive_expect_tx(&sfull[s], C::STATE_BYTES);
+            tma_load_state<StateT>(smem + (size_t)s * C::STATE_BYTES, &state_map, (blockIdx.x + js * P) % a.H,
+                                   slot_s, &sfull[s]);
+          } else {
+            mbar_arrive(&sfull[s]);
           }
         }
         __syncwarp();
@@ -396,54 +441,98 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
     return;
   }
 
-  if (warp > C::NW) {
-    // ---------------- prologue warps (units round-robin): conv + SiLU, cache shift, coefficients ----------------
-    for (int j = warp - C::NW - 1; j < n_my; j += fused_np<StateT>()) {
-      const int s = j % C::NSTAGE;
-      const bool ok = mbar_wait(&full[s], (j / C::NSTAGE) & 1);
+  if (warp == C::NW + 1 + C::NP) {
+    // ---------------- epilogue: gated RMSNorm of each unit, lane l on columns 4l..4l+3 ----------------
+    const float4 nw = __ldg(reinterpret_cast<const float4*>(a.norm_w) + lane);
+    for (int j = 0; j < n_my; ++j) {
+      const int e = j % C::NA;
+      const bool ok = mbar_wait(&odone[e], (j / C::NA) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) record_error(1u);
         return;
       }
-      const int4 sc = scal[s];
+      const int u = blockIdx.x + j * P;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)u * kD + 4 * lane;  // u = r * H + h
+      const unsigned char* act = entry(e);
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+      if (scal(e)->x >= 0) {
+        const float4 o = reinterpret_cast<const float4*>(act + F_O)[lane];
+        const float4 og = lds4(act + F_OG, 4 * lane, KDA_DT_BF16);
+        const float ss = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+        const float rinv = rsqrtf(ss * (1.f / kD) + a.norm_eps);
+        y[0] = o.x * rinv * nw.x * sigmoidf_(og.x);
+        y[1] = o.y * rinv * nw.y * sigmoidf_(og.y);
+        y[2] = o.z * rinv * nw.z * sigmoidf_(og.z);
+        y[3] = o.w * rinv * nw.w * sigmoidf_(og.w);
+      }
+      store_out<4>(out, y);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&aempty[e]);
+    }
+    return;
+  }
+
+  if (warp > C::NW) {
+    // ---------------- prologue warps (units round-robin): conv + SiLU, cache shift, coefficients ----------------
+    // Lane l works on channels 4l..4l+3 of each section (q, k, v), the layout
+    // of the coefficients.  The conv weights of a warp's next unit are loaded
+    // while it works on the current one: an L2 read under the stream's DRAM
+    // traffic takes about a microsecond.
+    const int p = warp - C::NW - 1;
+    float4 wv[3][4], wn[3][4];  // [section][tap]: current and next unit
+    auto load_weights = [&](float4 (&w)[3][4], int j) {
+      const int h = (blockIdx.x + j * P) % a.H;
+#pragma unroll
+      for (int sec = 0; sec < 3; ++sec)
+#pragma unroll
+        for (int tap = 0; tap < 4; ++tap)
+          w[sec][tap] = __ldg(reinterpret_cast<const float4*>(a.conv_w + (int64_t)(sec * 4 + tap) * HD + h * kD) + lane);
+    };
+    if (p < n_my) load_weights(wn, p);
+    for (int j = p; j < n_my; j += C::NP) {
+#pragma unroll
+      for (int sec = 0; sec < 3; ++sec)
+#pragma unroll
+        for (int tap = 0; tap < 4; ++tap) wv[sec][tap] = wn[sec][tap];
+      if (j + C::NP < n_my) load_weights(wn, j + C::NP);
+      const int e = j % C::NA;
+      const bool ok = mbar_wait(&afull[e], (j / C::NA) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) record_error(1u);
+        return;
+      }
+      const int4 sc = *scal(e);
       if (sc.x >= 0) {
-        const int u = blockIdx.x + j * P;
-        const int h = u % a.H;
-        const unsigned char* act = smem + (size_t)s * C::STAGE_BYTES + C::STATE_BYTES;
-        const __nv_bfloat16* xs = reinterpret_cast<const __nv_bfloat16*>(act + F_X);
-        const __nv_bfloat16* css = reinterpret_cast<const __nv_bfloat16*>(act + F_CS);
-        float* conv = conv_all + s * 3 * kD;
-        if (lane == 0) {
-          // The shifted cache [tap1, tap2, x] is already in the stage: nine bulk stores.
-          fence_proxy_async_smem();
-          __nv_bfloat16* csg = static_cast<__nv_bfloat16*>(a.conv_state) + (int64_t)sc.x * a.cs_slot_stride + h * kD;
+        const int h = (blockIdx.x + j * P) % a.H;
+        unsigned char* act = entry(e);
+        // Raw taps, oldest first, then x: four bf16 channels per lane and section.
+        // The shifted cache [tap1, tap2, x] goes back from registers.
+        __nv_bfloat16* csg = static_cast<__nv_bfloat16*>(a.conv_state) + (int64_t)sc.x * a.cs_slot_stride + h * kD +
+                             4 * lane;
+        float4 y[3];
 #pragma unroll
-          for (int sec = 0; sec < 3; ++sec) {
-            bulk_store(csg + sec * HD, act + F_CS + (1 * 3 + sec) * 256, 256);
-            bulk_store(csg + a.cs_tap_stride + sec * HD, act + F_CS + (2 * 3 + sec) * 256, 256);
-            bulk_store(csg + 2 * a.cs_tap_stride + sec * HD, act + F_X + sec * 256, 256);
+        for (int sec = 0; sec < 3; ++sec) {
+          uint2 t[4];
+#pragma unroll
+          for (int tap = 0; tap < 3; ++tap)
+            t[tap] = reinterpret_cast<const uint2*>(act + F_CS + (tap * 3 + sec) * 256)[lane];
+          t[3] = reinterpret_cast<const uint2*>(act + F_X + sec * 256)[lane];
+#pragma unroll
+          for (int tap = 1; tap < 4; ++tap)
+            *reinterpret_cast<uint2*>(csg + (int64_t)(tap - 1) * a.cs_tap_stride + sec * HD) = t[tap];
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int tap = 0; tap < 4; ++tap) {
+            const float4 w = wv[sec][tap];
+            acc.x = fmaf(w.x, bf_lo(t[tap].x), acc.x);
+            acc.y = fmaf(w.y, bf_hi(t[tap].x), acc.y);
+            acc.z = fmaf(w.z, bf_lo(t[tap].y), acc.z);
+            acc.w = fmaf(w.w, bf_hi(t[tap].y), acc.w);
           }
-          bulk_commit();
+          y[sec] = make_float4(acc.x * sigmoidf_(acc.x), acc.y * sigmoidf_(acc.y), acc.z * sigmoidf_(acc.z),
+                               acc.w * sigmoidf_(acc.w));
         }
-        float wv[12][4];  // all the head's conv weights in flight at once
-#pragma unroll
-        for (int i = 0; i < 12; ++i) {
-          const int sec = i >> 2, c = (lane + 32 * i) & (kD - 1);
-          const float* w = a.conv_w + (int64_t)sec * 4 * HD + h * kD + c;
-#pragma unroll
-          for (int tap = 0; tap < 4; ++tap) wv[i][tap] = __ldg(w + tap * HD);
-        }
-#pragma unroll
-        for (int i = 0; i < 12; ++i) {  // channel lc = lane + 32 i of the head's 384
-          const int lc = lane + 32 * i;
-          const int sec = i >> 2, c = lc & (kD - 1);
-          float y = wv[i][0] * __bfloat162float(css[(0 * 3 + sec) * kD + c]);
-          y = fmaf(wv[i][1], __bfloat162float(css[(1 * 3 + sec) * kD + c]), y);
-          y = fmaf(wv[i][2], __bfloat162float(css[(2 * 3 + sec) * kD + c]), y);
-          y = fmaf(wv[i][3], __bfloat162float(xs[lc]), y);
-          conv[lc] = y * sigmoidf_(y);
-        }
-        __syncwarp();
+        reinterpret_cast<float4*>(act + F_V)[lane] = y[2];  // v, read by the consumers
         const float A = __int_as_float(sc.z);
         const float4 gr = lds4(act + F_G, 4 * lane, KDA_DT_BF16);
         const float4 dtb = reinterpret_cast<const float4*>(act + F_DT)[lane];
@@ -452,93 +541,67 @@ __global__ void __launch_bounds__((FusedStream<StateT>::NW + 1 + fused_np<StateT
         d.y = expf(log_decay(gr.y + dtb.y, A, a.gate_mode, a.lower_bound));
         d.z = expf(log_decay(gr.z + dtb.z, A, a.gate_mode, a.lower_bound));
         d.w = expf(log_decay(gr.w + dtb.w, A, a.gate_mode, a.lower_bound));
-        const float4 q = reinterpret_cast<const float4*>(conv)[lane];
-        const float4 k = reinterpret_cast<const float4*>(conv + kD)[lane];
-        const float qk = token_coefficients(q, k, d, lane, coef_all + s * kD);
-        if (lane == 0) scal[s].w = __float_as_int(qk);
+        const float qk = token_coefficients(y[0], y[1], d, lane, reinterpret_cast<float4*>(act + F_COEF));
+        if (lane == 0) scal(e)->w = __float_as_int(qk);
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&ready[s]);
-        bulk_wait_read();  // the cache write-back no longer reads the stage
-        mbar_arrive(&empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&aready[e]);
     }
-    if (lane == 0) bulk_wait_all();
     return;
   }
 
   // ---------------- consumers ----------------
   const int col0 = warp * C::CW + (lane % G::LPR) * G::VEC;
   const int row0 = stream_row0<G::LPR>(lane);
-  float nw[G::VEC];
-#pragma unroll
-  for (int jj = 0; jj < G::VEC; ++jj) nw[jj] = __ldg(a.norm_w + col0 + jj);
   for (int j = 0; j < n_my; ++j) {
-    const int s = j % C::NSTAGE;
-    const uint32_t par = (j / C::NSTAGE) & 1;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], par) && mbar_wait(&ready[s], par));
-    const int u = blockIdx.x + j * P;
-    const int h = u % a.H, r = u / a.H;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)r * a.H + h) * kD;
-    const int4 sc = ok ? scal[s] : make_int4(-1, 0, 0, 0);
-    const bool live = ok && sc.x >= 0;
-    float o[G::VEC], og[G::VEC];
-    float ss = 0.f;
-    if (live) {
-      const unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
-      const float4* coef = coef_all + s * kD;
-      const float* conv = conv_all + s * 3 * kD;
+    const int s = j % C::NS, e = j % C::NA;
+    const bool ok = mbar_wait(&sfull[s], (j / C::NS) & 1) && mbar_wait(&afull[e], (j / C::NA) & 1) &&
+                    mbar_wait(&aready[e], (j / C::NA) & 1);
+    if (!__all_sync(0xffffffffu, ok)) {
+      if (lane == 0) record_error(1u);
+      return;
+    }
+    const int4 sc = *scal(e);
+    unsigned char* act = entry(e);
+    if (sc.x >= 0) {
+      const int h = (blockIdx.x + j * P) % a.H;
+      const unsigned char* st = smem + (size_t)s * C::STATE_BYTES;
       float vv[G::VEC];
 #pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = conv[2 * kD + col0 + jj];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; jj += 4) {
-        const float4 t = lds4(st + C::STATE_BYTES + F_OG, col0 + jj, KDA_DT_BF16);
-        og[jj] = t.x; og[jj + 1] = t.y; og[jj + 2] = t.z; og[jj + 3] = t.w;
-      }
+      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = reinterpret_cast<const float*>(act + F_V)[col0 + jj];
       typename Frag<StateT>::Raw S[G::PASSES];
       float2 dk[G::PASSES];
       float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
-      reduce_stage<StateT, G>(st, coef, row0, col0, S, dk, acc2_a, acc2_b);
+      reduce_stage<StateT, G>(st, reinterpret_cast<const float4*>(act + F_COEF), row0, col0, S, dk, acc2_a, acc2_b);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
+      if (lane == 0) mbar_arrive(&sempty[s]);
       float acc_a[G::VEC], acc_b[G::VEC];
       strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
       const float beta = __int_as_float(sc.y);
       const float qk = __int_as_float(sc.w);
       float u_[G::VEC];
 #pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) {
-        u_[jj] = beta * (vv[jj] - acc_a[jj]);
-        o[jj] = a.scale * (acc_b[jj] + qk * u_[jj]);
-        ss = fmaf(o[jj], o[jj], ss);
+      for (int jj = 0; jj < G::VEC; ++jj) u_[jj] = beta * (vv[jj] - acc_a[jj]);
+      if (row0 == 0) {  // these lanes hold distinct columns: o before the norm, for the epilogue warp
+#pragma unroll
+        for (int jj = 0; jj < G::VEC; jj += 4)
+          reinterpret_cast<float4*>(act + F_O)[(col0 + jj) / 4] =
+              make_float4(a.scale * (acc_b[jj] + qk * u_[jj]), a.scale * (acc_b[jj + 1] + qk * u_[jj + 1]),
+                          a.scale * (acc_b[jj + 2] + qk * u_[jj + 2]), a.scale * (acc_b[jj + 3] + qk * u_[jj + 3]));
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&odone[e]);
+        mbar_arrive(&aempty[e]);
       }
       StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
       update_store_regs<StateT, G>(sp, row0, col0, S, dk, u_);
-    } else if (ok) {
+    } else {
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
-    }
-    // RMS over the 128 value columns: lanes with row0 == 0 hold distinct columns.
-    ss = warp_sum(row0 == 0 ? ss : 0.f);
-    if (lane == 0) s_ss[(j & 1) * C::NW + warp] = ss;
-    if (!bar_and(1, C::NW * 32, ok)) {  // one departed warp takes all consumers out
-      if (!ok && lane == 0) record_error(1u);
-      return;
-    }
-    if (row0 == 0) {
-      if (live) {
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < C::NW; ++w) tot += s_ss[(j & 1) * C::NW + w];
-        const float rinv = rsqrtf(tot * (1.f / kD) + a.norm_eps);
-        float y[G::VEC];
-#pragma unroll
-        for (int jj = 0; jj < G::VEC; ++jj) y[jj] = o[jj] * rinv * nw[jj] * sigmoidf_(og[jj]);
-        store_out<G::VEC>(out + col0, y);
-      } else {
-        store_out_zero<G::VEC>(out + col0);
+      if (lane == 0) {
+        mbar_arrive(&sempty[s]);
+        mbar_arrive(&odone[e]);
+        mbar_arrive(&aempty[e]);
       }
     }
   }
@@ -602,7 +665,7 @@ cudaError_t launch_fused_stream_typed(const FusedArgs& a, int sm_count, cudaStre
   const int units = a.rows * a.H;
   const int grid = units < sm_count ? units : sm_count;
   return launch_pdl(kda_fused_stream_kernel<StateT>, dim3(grid),
-                    dim3((FusedStream<StateT>::NW + 1 + fused_np<StateT>()) * 32), smem, s, 1, a, map, units);
+                    dim3(FusedRing<StateT>::WARPS * 32), smem, s, 1, a, map, units);
 }
 
 }  // namespace

@@ -1,7 +1,6 @@
 // Shared pieces of the persistent streaming kernels: stage geometry, the
 // 128-byte swizzle of TMA-loaded state blocks, shared-memory activation
-// reads, the 3-d tensor-map load, named-barrier votes, and the tensor-map
-// encoder entry point.
+// reads, the 3-d tensor-map load, and the tensor-map encoder entry point.
 #pragma once
 
 #include <cuda.h>
@@ -99,20 +98,6 @@ __device__ __forceinline__ void tma_load_state(unsigned char* dst, const CUtenso
   using C = SwzCfg<StateT>;
 #pragma unroll
   for (int blk = 0; blk < C::NBLK; ++blk) tma_load_3d(dst + blk * C::BLK_BYTES, map, blk * C::BLK_COLS, h * kD, slot, bar);
-}
-
-// Named barrier `id` over `nthreads` threads with an AND vote of `ok`.
-__device__ __forceinline__ bool bar_and(int id, int nthreads, bool ok) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred q, p;\n\t"
-      "setp.ne.u32 q, %1, 0;\n\t"
-      "barrier.cta.red.and.pred p, %2, %3, q;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)ok), "r"(id), "r"(nthreads)
-      : "memory");
-  return r != 0;
 }
 
 // ---- host side -----------------------------------------------------------------------

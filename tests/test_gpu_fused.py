@@ -183,6 +183,38 @@ def test_fused_stream_rejects_unaligned_rows(stream_schedule):
     assert e.value.status == 2
 
 
+def _unaligned_weight(d):
+    flat = torch.zeros(d["conv_weight"].numel() + 1, dtype=torch.float32, device="cuda")
+    flat[1:] = d["conv_weight"].reshape(-1)
+    w = flat[1:].view(d["conv_weight"].shape)
+    assert w.data_ptr() % 16 != 0
+    return w
+
+
+def test_fused_stream_rejects_unaligned_conv_weight(stream_schedule):
+    """The streaming prologue reads four weights per lane at once."""
+    case = synth.fused_case(8, 4, seed=34)
+    d = _device_case(case)
+    d["conv_weight"] = _unaligned_weight(d)
+    with pytest.raises(binding.KdaError) as e:
+        _run(d)
+    assert e.value.status == 2
+
+
+def test_fused_unaligned_conv_weight_falls_back_to_split():
+    """A batch the dispatcher would stream (32 x 32 units), with conv_weight
+    4 bytes off a 16-byte boundary: the call takes the split kernel."""
+    H, rows = 32, 32
+    case = synth.fused_case(H, rows, seed=35, null_frac=0.1)
+    d = _device_case(case)
+    d["conv_weight"] = _unaligned_weight(d)
+    before, cbefore = d["state"].clone(), d["conv_state"].clone()
+    out = _run(d)
+    torch.cuda.synchronize()
+    _check(case, d, before, cbefore, out)
+    assert binding.kda_device_error() == 0
+
+
 @pytest.mark.parametrize("cluster", [1, 2, 4])
 @pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("lower_bound", [-5.0, None])
