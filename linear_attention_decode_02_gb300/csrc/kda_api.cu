@@ -263,8 +263,9 @@ kda_status current_device(cudaStream_t stream, DeviceInfo* info) {
 //    ~95% of copy bandwidth at B >= 128 and beats the streaming kernel;
 //  - bfloat16 state, T=1: the streaming kernel once the units fill five per
 //    SM (packed K3 B >= 64), the split kernel below;
-//  - fused: the streaming kernel from five units per SM (H=32 rows=256
-//    fp32: 88 % vs 68 % split; rows=32: 59 % vs 52 %), split below;
+//  - fused: the streaming kernel from 2.5 units per SM (H=32 rows=12:
+//    14.4 vs 15.8 us split, fp32; rows=256: 164.8 us, 91 % of copy
+//    bandwidth), split below (rows=8: 11.3 vs 12.4 us);
 //  - speculative rows: the split kernel, except a bfloat16 state with
 //    t_max >= 14, which takes the tensor-core chunked form (N=128, rows of
 //    exactly T tokens: T=14 102.5 vs 129.6 us, T=16 104.6 vs 142.1 us;
@@ -281,7 +282,7 @@ int plan_schedule(int op, int64_t units, int state_dtype, int t_max, int sms) {
   }
   if (forced == KDA_SCHED_SPLIT || forced == KDA_SCHED_STREAM) return forced;
   if (g_split_override.load() != 0) return KDA_SCHED_SPLIT;
-  if (op == KDA_OP_FUSED) return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
+  if (op == KDA_OP_FUSED) return 2 * units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
   if (state_dtype == KDA_F32) return KDA_SCHED_SPLIT;
   return units >= 5LL * sms ? KDA_SCHED_STREAM : KDA_SCHED_SPLIT;
 }

@@ -428,6 +428,8 @@ def test_schedule_override_and_plan(lib):
     assert binding.kda_plan_schedule(0, 16384, 1, 1, 152) == 2  # bf16 state: stream
     assert binding.kda_plan_schedule(2, 8192, 0, 1, 152) == 2  # fused, many units
     assert binding.kda_plan_schedule(2, 1024, 0, 1, 152) == 2
+    assert binding.kda_plan_schedule(2, 380, 0, 1, 152) == 2  # from 2.5 units per SM
+    assert binding.kda_plan_schedule(2, 379, 1, 1, 152) == 1
     assert binding.kda_plan_schedule(2, 256, 0, 1, 152) == 1
     # speculative rows: the tensor-core form for a bf16 state with t_max >= 14
     assert binding.kda_plan_schedule(3, 2048, 1, 14, 152) == 3
