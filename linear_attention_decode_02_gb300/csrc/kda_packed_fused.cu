@@ -78,38 +78,6 @@ __device__ __forceinline__ float token_coefficient_pairs(float4 q, float4 k, flo
 // value; gives 0 where e^-x overflows.
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
-// Column sums of a 16-column strip's two k-reductions by reduce-scatter over
-// the strip's RPI row groups (2 VEC of them): at each level a lane keeps one
-// half of its values and adds its partner's copy of that half, so the lane of
-// row group rg ends holding value rg of (a_0 .. a_{VEC-1}, b_0 .. b_{VEC-1})
-// summed over all rows, after RPI - 1 shuffles instead of log2(RPI) * 2 VEC.
-template <typename G>
-__device__ __forceinline__ float strip_reduce_scatter(const float2 (&a2)[G::VEC / 2], const float2 (&b2)[G::VEC / 2],
-                                                      int rg) {
-  constexpr int NV = 2 * G::VEC;
-  static_assert(NV == G::RPI, "one value per row group");
-  float v[NV];
-#pragma unroll
-  for (int p = 0; p < G::VEC / 2; ++p) {
-    v[2 * p] = a2[p].x; v[2 * p + 1] = a2[p].y;
-    v[G::VEC + 2 * p] = b2[p].x; v[G::VEC + 2 * p + 1] = b2[p].y;
-  }
-  constexpr int LEVELS = NV == 8 ? 3 : (NV == 16 ? 4 : 0);
-  static_assert(LEVELS > 0, "8 or 16 row groups");
-#pragma unroll
-  for (int l = 0; l < LEVELS; ++l) {
-    const int half = NV >> (l + 1);
-    const int bit = LEVELS - 1 - l;  // the row-group bit of this level, most significant first
-    const bool hi = (rg >> bit) & 1;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = hi ? v[i] : v[i + half];
-      const float keep = hi ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, G::LPR << bit);
-    }
-  }
-  return v[0];
-}
 
 }  // namespace
 

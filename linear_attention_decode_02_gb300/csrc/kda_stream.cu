@@ -56,6 +56,11 @@ __device__ __forceinline__ void reduce_stage(const unsigned char* st, const floa
   }
 }
 
+// The column sums by reduce-scatter (strip_reduce_scatter) where a strip has
+// 2 VEC row groups, i.e. with a bf16 state: 24 shuffles instead of 64.
+template <typename StateT, typename G>
+constexpr bool kStreamScatter = sizeof(StateT) == 2 && 2 * G::VEC == G::RPI;
+
 // S' = d S + k u^T from the registers of reduce_stage, stored to global.
 template <typename StateT, typename G>
 __device__ __forceinline__ void update_store_regs(StateT* sp, int row0, int col0,
@@ -246,13 +251,24 @@ __global__ void __launch_bounds__((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PART
       continue;
     }
     const unsigned char* st = smem + (size_t)s * C::STAGE_BYTES;
+    const unsigned char* vact = st + C::PART_BYTES + 2 * T1_ACT_SLOT;
     const float4* coef = coef_all + s * kD;
     float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
+    // v before the stage is released: the lane's VEC columns, or with the
+    // scatter the one column its row group forms u for
+    const int rg = lane / G::LPR;
     float vv[G::VEC];
+    if constexpr (kStreamScatter<StateT, G>) {
+      vv[0] = rg < G::VEC ? (a.qkv_dtype == KDA_DT_F32
+                                 ? reinterpret_cast<const float*>(vact)[gcol + rg]
+                                 : __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(vact)[gcol + rg]))
+                          : 0.f;
+    } else {
 #pragma unroll
-    for (int jj = 0; jj < G::VEC; jj += 4) {
-      const float4 t = lds4(st + C::PART_BYTES + 2 * T1_ACT_SLOT, gcol + jj, a.qkv_dtype);
-      vv[jj] = t.x; vv[jj + 1] = t.y; vv[jj + 2] = t.z; vv[jj + 3] = t.w;
+      for (int jj = 0; jj < G::VEC; jj += 4) {
+        const float4 t = lds4(vact, gcol + jj, a.qkv_dtype);
+        vv[jj] = t.x; vv[jj + 1] = t.y; vv[jj + 2] = t.z; vv[jj + 3] = t.w;
+      }
     }
     // k-reductions; the decay and key coefficients of each row stay in registers
     typename Frag<StateT>::Raw S[G::PASSES];
@@ -260,19 +276,31 @@ __global__ void __launch_bounds__((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PART
     reduce_stage<StateT, G>(st, coef, row0, col0, S, dk, acc2_a, acc2_b);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[s]);  // this warp no longer reads the stage
-    float acc_a[G::VEC], acc_b[G::VEC];
-    strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
     const float beta = __int_as_float(sc.y);
     const float qk = __int_as_float(sc.w);
-    float u_[G::VEC], o[G::VEC];
+    float u_[G::VEC];
+    if constexpr (kStreamScatter<StateT, G>) {
+      // bf16 (16 row groups): the lane of row group rg < VEC forms u for
+      // column rg of its VEC, the lane VEC groups up forms o for it and
+      // writes it; every lane then gathers the VEC u
+      const float tot = strip_reduce_scatter<G>(acc2_a, acc2_b, rg);
+      const float uc = rg < G::VEC ? beta * (vv[0] - tot) : 0.f;
+      const float u_lo = __shfl_xor_sync(0xffffffffu, uc, G::LPR * G::VEC);
+      if (rg >= G::VEC) out[gcol + rg - G::VEC] = __float2bfloat16_rn(a.scale * (tot + qk * u_lo));
 #pragma unroll
-    for (int jj = 0; jj < G::VEC; ++jj) {
-      u_[jj] = beta * (vv[jj] - acc_a[jj]);
-      o[jj] = a.scale * (acc_b[jj] + qk * u_[jj]);
+      for (int c = 0; c < G::VEC; ++c) u_[c] = __shfl_sync(0xffffffffu, uc, c * G::LPR + lane % G::LPR);
+    } else {
+      float acc_a[G::VEC], acc_b[G::VEC], o[G::VEC];
+      strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
+#pragma unroll
+      for (int jj = 0; jj < G::VEC; ++jj) {
+        u_[jj] = beta * (vv[jj] - acc_a[jj]);
+        o[jj] = a.scale * (acc_b[jj] + qk * u_[jj]);
+      }
+      if (row0 == 0) store_out<G::VEC>(out + gcol, o);
     }
     StateT* sp = static_cast<StateT*>(a.state) + (int64_t)sc.x * a.slot_stride + (int64_t)h * kD * kD;
     update_store_regs<StateT, G>(sp, row0, gcol, S, dk, u_);
-    if (row0 == 0) store_out<G::VEC>(out + gcol, o);
   }
 }
 
@@ -566,28 +594,37 @@ __global__ void __launch_bounds__(FusedRing<StateT>::WARPS * 32, 1)
     if (sc.x >= 0) {
       const int h = (blockIdx.x + j * P) % a.H;
       const unsigned char* st = smem + (size_t)s * C::STATE_BYTES;
-      float vv[G::VEC];
-#pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) vv[jj] = reinterpret_cast<const float*>(act + F_V)[col0 + jj];
+      const float* vf = reinterpret_cast<const float*>(act + F_V);
+      float* of = reinterpret_cast<float*>(act + F_O);  // o before the norm, for the epilogue warp
       typename Frag<StateT>::Raw S[G::PASSES];
       float2 dk[G::PASSES];
       float2 acc2_a[G::VEC / 2], acc2_b[G::VEC / 2];
       reduce_stage<StateT, G>(st, reinterpret_cast<const float4*>(act + F_COEF), row0, col0, S, dk, acc2_a, acc2_b);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[s]);
-      float acc_a[G::VEC], acc_b[G::VEC];
-      strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
       const float beta = __int_as_float(sc.y);
       const float qk = __int_as_float(sc.w);
       float u_[G::VEC];
+      if constexpr (kStreamScatter<StateT, G>) {  // as in the T=1 kernel
+        const int rg = lane / G::LPR;
+        const float tot = strip_reduce_scatter<G>(acc2_a, acc2_b, rg);
+        const float uc = rg < G::VEC ? beta * (vf[col0 + rg] - tot) : 0.f;
+        const float u_lo = __shfl_xor_sync(0xffffffffu, uc, G::LPR * G::VEC);
+        if (rg >= G::VEC) of[col0 + rg - G::VEC] = a.scale * (tot + qk * u_lo);
 #pragma unroll
-      for (int jj = 0; jj < G::VEC; ++jj) u_[jj] = beta * (vv[jj] - acc_a[jj]);
-      if (row0 == 0) {  // these lanes hold distinct columns: o before the norm, for the epilogue warp
+        for (int c = 0; c < G::VEC; ++c) u_[c] = __shfl_sync(0xffffffffu, uc, c * G::LPR + lane % G::LPR);
+      } else {
+        float acc_a[G::VEC], acc_b[G::VEC];
+        strip_allreduce<G>(acc2_a, acc2_b, acc_a, acc_b);
 #pragma unroll
-        for (int jj = 0; jj < G::VEC; jj += 4)
-          reinterpret_cast<float4*>(act + F_O)[(col0 + jj) / 4] =
-              make_float4(a.scale * (acc_b[jj] + qk * u_[jj]), a.scale * (acc_b[jj + 1] + qk * u_[jj + 1]),
-                          a.scale * (acc_b[jj + 2] + qk * u_[jj + 2]), a.scale * (acc_b[jj + 3] + qk * u_[jj + 3]));
+        for (int jj = 0; jj < G::VEC; ++jj) u_[jj] = beta * (vf[col0 + jj] - acc_a[jj]);
+        if (row0 == 0) {  // these lanes hold distinct columns
+#pragma unroll
+          for (int jj = 0; jj < G::VEC; jj += 4)
+            reinterpret_cast<float4*>(of)[(col0 + jj) / 4] =
+                make_float4(a.scale * (acc_b[jj] + qk * u_[jj]), a.scale * (acc_b[jj + 1] + qk * u_[jj + 1]),
+                            a.scale * (acc_b[jj + 2] + qk * u_[jj + 2]), a.scale * (acc_b[jj + 3] + qk * u_[jj + 3]));
+        }
       }
       __syncwarp();
       if (lane == 0) {
