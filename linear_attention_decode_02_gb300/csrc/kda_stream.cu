@@ -374,7 +374,9 @@ __global__ void __launch_bounds__(FusedRing<StateT>::WARPS * 32, 1)
     for (int e = 0; e < C::NA; ++e) {
       mbar_init(&afull[e], 1);
       mbar_init(&aready[e], 1);
-      mbar_init(&aempty[e], C::NW + 1);  // the prologue is done reading an entry before it marks it ready
+      // consumers + the epilogue warp; the prologue has finished reading the
+      // entry before it marks it ready, so it need not arrive
+      mbar_init(&aempty[e], C::NW + 1);
       mbar_init(&odone[e], C::NW);
     }
     mbar_fence_init();
