@@ -144,10 +144,13 @@ def test_fused_stream_parity(stream_schedule, state_dtype, lower_bound, H, rows)
     assert binding.kda_device_error() == 0
 
 
-def test_fused_stream_many_units_and_graph(stream_schedule):
-    """Many rounds through every stage, under graph replay with new inputs."""
+@pytest.mark.parametrize("state_dtype", [torch.float32, torch.bfloat16])
+def test_fused_stream_many_units_and_graph(stream_schedule, state_dtype):
+    """Many rounds through both rings (about 16 units a CTA: the activation
+    entries run ahead of the state stages and wrap several times), under
+    graph replay with new inputs."""
     H, rows = 8, 300
-    c1 = synth.fused_case(H, rows, seed=31, null_frac=0.1)
+    c1 = synth.fused_case(H, rows, seed=31, null_frac=0.1, state_dtype=state_dtype)
     d = _device_case(c1)
     out = torch.empty(1, rows, H, 128, dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()
@@ -158,7 +161,7 @@ def test_fused_stream_many_units_and_graph(stream_schedule):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
         _run(d, out=out)
-    c2 = synth.fused_case(H, rows, seed=32, null_frac=0.15)
+    c2 = synth.fused_case(H, rows, seed=32, null_frac=0.15, state_dtype=state_dtype)
     for key in ("x", "raw_gate", "raw_beta", "output_gate", "state_indices", "state"):
         d[key].copy_(c2[key].cuda())
     d["conv_state"].copy_(c2["conv_state"].cuda())

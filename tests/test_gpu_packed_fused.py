@@ -128,15 +128,23 @@ def test_packed_fused_softplus_gate_and_head_counts():
         _check(case, d, st0, cs0, out, lower_bound=None)
 
 
-def test_packed_fused_null_checkpoints_and_bad_accepted_counts():
-    case = synth.packed_fused_case(4, 3, H=3, seed=32, lengths=[3, 3, 2, 3], accepted=[1, 2, 4, 0])
+@pytest.mark.parametrize("state_dtype,cluster", [(torch.float32, 0), (torch.bfloat16, 1)])
+def test_packed_fused_null_checkpoints_and_bad_accepted_counts(state_dtype, cluster):
+    """Skipped, null and out-of-range checkpoint slots; with a bf16 state and
+    one CTA per unit the checkpoints leave by TMA stores."""
+    case = synth.packed_fused_case(4, 3, H=3, seed=32, lengths=[3, 3, 2, 3], accepted=[1, 2, 4, 0],
+                                   state_dtype=state_dtype)
     case["state_indices"][0, 1] = -1   # checkpoint 1 of sequence 0 not kept
     case["state_indices"][1, 1] = 0    # sequence 1 starts from the null slot
     case["state_indices"][0, 2] = 10 ** 6  # out of range: skipped
     d, st0, cs0 = _setup(case)
     out = torch.full((case["x"].shape[0], 3, 128), 7.0, dtype=torch.bfloat16, device="cuda")
-    _run(d, out=out)
-    torch.cuda.synchronize()
+    binding.kda_set_split_override(cluster)
+    try:
+        _run(d, out=out)
+        torch.cuda.synchronize()
+    finally:
+        binding.kda_set_split_override(0)
     _check(case, d, st0, cs0, out)
 
 
