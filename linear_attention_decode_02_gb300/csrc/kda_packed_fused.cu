@@ -29,11 +29,15 @@ __device__ __forceinline__ void cp_async4(void* dst_smem, const void* src) {
                : "memory");
 }
 // Shared -> global TMA tensor store of one box at coordinates (x, y, z),
-// completing in the issuing thread's bulk group.
+// completing in the issuing thread's bulk group.  The lines are marked
+// evict-first in L2 (nothing in the call reads a checkpoint back), as the
+// streaming stores of the plain path are: H=12 N=128 76.9 -> 75.3 us.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
-  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
-               "r"(static_cast<uint32_t>(__cvta_generic_to_shared(src))), "r"(x), "r"(y), "r"(z)
+               "r"(static_cast<uint32_t>(__cvta_generic_to_shared(src))), "r"(x), "r"(y), "r"(z), "l"(policy)
                : "memory");
 }
 // Hint: bring the 128-byte line holding `p` (a global address) into L2.
