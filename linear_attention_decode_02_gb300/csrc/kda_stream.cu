@@ -476,7 +476,8 @@ __global__ void __launch_bounds__(FusedRing<StateT>::WARPS * 32, 1)
     const float4 nw = __ldg(reinterpret_cast<const float4*>(a.norm_w) + lane);
     for (int j = 0; j < n_my; ++j) {
       const int e = j % C::NA;
-      const bool ok = mbar_wait(&odone[e], (j / C::NA) & 1);
+      // the output gate arrived by bulk copy on the entry's afull barrier
+      const bool ok = mbar_wait(&odone[e], (j / C::NA) & 1) && mbar_wait(&afull[e], (j / C::NA) & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         if (lane == 0) record_error(1u);
         return;
