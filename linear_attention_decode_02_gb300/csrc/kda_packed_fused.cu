@@ -82,7 +82,6 @@ __device__ __forceinline__ float token_coefficient_pairs(float4 q, float4 k, flo
 // value; gives 0 where e^-x overflows.
 __device__ __forceinline__ float sigmoid_fast(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
-
 }  // namespace
 
 // =====================================================================================
