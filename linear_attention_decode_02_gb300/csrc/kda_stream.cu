@@ -230,7 +230,15 @@ __global__ void __launch_bounds__((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PART
   // ---------------- consumers: group warp / GROUP_WARPS takes items j = group, group + PARTS, ... ----------------
   const int col0 = (warp % C::GROUP_WARPS) * C::CW + (lane % G::LPR) * G::VEC;  // column within the staged part
   const int row0 = stream_row0<G::LPR>(lane);
-  for (int j = warp / C::GROUP_WARPS; j < n_my; j += PARTS) {
+  // The unit advances by P from one of this group's items to the next, so
+  // with a bf16 state (whose consumers set the pace) its head is kept by one
+  // conditional subtraction instead of a division; the float32 kernel, at its
+  // register cap, divides.
+  constexpr bool kStepH = sizeof(StateT) == 2;
+  const int h_step = P % a.H;
+  int h_run = (int)(((blockIdx.x + (warp / C::GROUP_WARPS) * P) / PARTS) % a.H);
+  for (int j = warp / C::GROUP_WARPS; j < n_my;
+       j += PARTS, h_run = h_run + h_step >= a.H ? h_run + h_step - a.H : h_run + h_step) {
     const int s = j % C::NSTAGE;
     const uint32_t par = (j / C::NSTAGE) & 1;
     const bool ok = mbar_wait(&full[s], par) && mbar_wait(&ready[s], par);
@@ -241,8 +249,8 @@ __global__ void __launch_bounds__((T1StreamP<StateT, PARTS>::NW + 1 + t1_np<PART
     const int item = blockIdx.x + j * P;
     const int u = item / PARTS;
     const int gcol = (item % PARTS) * C::PART_COLS + col0;  // column within the unit
-    const int h = u % a.H, b = u / a.H;
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)b * a.H + h) * kD;
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (int64_t)u * kD;  // u = b * H + h
+    const int h = kStepH ? h_run : u % a.H;
     const int4 sc = scal[s];
     if (sc.x < 0) {  // null row: zero output, no cache access
       if (row0 == 0) store_out_zero<G::VEC>(out + gcol);
@@ -584,7 +592,11 @@ __global__ void __launch_bounds__(FusedRing<StateT>::WARPS * 32, 1)
   // ---------------- consumers ----------------
   const int col0 = warp * C::CW + (lane % G::LPR) * G::VEC;
   const int row0 = stream_row0<G::LPR>(lane);
-  for (int j = 0; j < n_my; ++j) {
+  // the unit advances by P: with a bf16 state its head without a division
+  constexpr bool kStepH = sizeof(StateT) == 2;
+  const int h_step = P % a.H;
+  int h_run = (int)(blockIdx.x % a.H);
+  for (int j = 0; j < n_my; ++j, h_run = h_run + h_step >= a.H ? h_run + h_step - a.H : h_run + h_step) {
     const int s = j % C::NS, e = j % C::NA;
     const bool ok = mbar_wait(&sfull[s], (j / C::NS) & 1) && mbar_wait(&afull[e], (j / C::NA) & 1) &&
                     mbar_wait(&aready[e], (j / C::NA) & 1);
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(FusedRing<StateT>::WARPS * 32, 1)
     const int4 sc = *scal(e);
     unsigned char* act = entry(e);
     if (sc.x >= 0) {
-      const int h = (blockIdx.x + j * P) % a.H;
+      const int h = kStepH ? h_run : (int)((blockIdx.x + j * P) % a.H);
       const unsigned char* st = smem + (size_t)s * C::STATE_BYTES;
       const float* vf = reinterpret_cast<const float*>(act + F_V);
       float* of = reinterpret_cast<float*>(act + F_O);  // o before the norm, for the epilogue warp
